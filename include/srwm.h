@@ -1,0 +1,127 @@
+/*
+ * srwm.h -- C ABI of libsrwm.so: the forward recurrence of the multi-head
+ * Self-Referential Weight Matrix (SRWM), hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence b and head h, steps t = 0 .. T-1) is the SRWM of
+ * "Metalearning Continual Learning Algorithms", section 2.3:
+ *   Eq. (1)  [y_t, k_t, q_t, beta_t] = W_{t-1} x~_t
+ *   Eq. (2)  v_t = W_{t-1} phi(q_t),   vbar_t = W_{t-1} phi(k_t)
+ *   Eq. (3)  W_t = W_{t-1} + sigma(beta_t) (v_t - vbar_t) (outer) phi(k_t)
+ * with phi = softmax, sigma = sigmoid, and x~_t = x_t (supervised variant) or
+ * softmax(x_t) over the head's d inputs (RL variant).  In the four-learning-rate
+ * version (same page, Eqs. (4)-(5)) W has row blocks [W^y; W^k; W^q; W^b] and
+ * beta_t = [b^y, b^k, b^q, b^b]; rows of block X use sigma(b^X), the four beta
+ * rows use sigma(b^b).  y_t comes from the pre-update matrix W_{t-1} (review of
+ * "A Modern Self-Referential Weight Matrix That Learns to Modify Itself",
+ * section 2.2).  Heads are independent, each on its own d coordinates of the
+ * D = H*d wide input (same review, section 2.4); W_0 is shared by all sequences.
+ *
+ * Shapes: per head d_in = d_out = d, W has m = 3*d + n_lr rows and d columns,
+ * stored row-major (row = output index), blocks in the order y, k, q, beta.
+ *
+ * Common rules for every entry point below:
+ *   - Pointers are DEVICE memory (cudaMalloc'd or managed) of fp32, contiguous,
+ *     16-byte aligned.  The caller owns all buffers; the library allocates
+ *     nothing and keeps no state except one device status word.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting.  Argument errors are
+ *     returned before anything is enqueued; nothing is written then.
+ *   - Supported: d in {16, 32, 64}, n_lr in {1, 4}, softmax_input in {0, 1}.
+ *   - Outputs must not overlap inputs or each other (srwm_step alone allows
+ *     W_out == W_in exactly, for an in-place update).
+ *   - Results are deterministic: the same inputs give the same bits.
+ */
+#ifndef SRWM_H
+#define SRWM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum srwm_status {
+    SRWM_OK = 0,
+    SRWM_ERR_NULL = 1,        /* a required pointer is NULL                               */
+    SRWM_ERR_SHAPE = 2,       /* B, H or d <= 0, T < 0, or a size overflows the layout    */
+    SRWM_ERR_UNSUPPORTED = 3, /* d not in {16,32,64}, n_lr not in {1,4}, bad flag value   */
+    SRWM_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned                         */
+    SRWM_ERR_ALIAS = 5,       /* an output overlaps an input or another output            */
+    SRWM_ERR_CUDA = 6,        /* a CUDA runtime call failed (launch, attribute, ...)      */
+    SRWM_ERR_TIMEOUT = 7,     /* a kernel gave up a bounded wait (see srwm_last_device_status) */
+    SRWM_ERR_NOT_DEVICE = 8   /* a pointer is not device-accessible CUDA memory           */
+};
+
+/*
+ * srwm_forward -- run T steps of Eqs. (1)-(3) (n_lr = 1) or Eqs. (4)-(5)
+ * (n_lr = 4) for every (sequence, head) stream, starting from the shared W0.
+ *
+ *   x        [B, T, H, d]  inputs; step t of stream (b, h) is x[b, t, h, :]
+ *   W0       [H, m, d]     initial matrix of each head, shared over b (read only)
+ *   B, T, H  batch, steps, heads; T == 0 is valid and copies W0 into W_final
+ *   d        per-head width (16, 32 or 64)
+ *   n_lr     1 (one learning rate, m = 3d+1) or 4 (four learning rates, m = 3d+4)
+ *   softmax_input  0: x~_t = x_t;  1: x~_t = softmax(x_t) over the head's d inputs
+ *   y_out    [B, T, H, d]  written: y_t of every stream
+ *   W_final  [B, H, m, d]  written: W_T of every stream
+ *   stream   cudaStream_t or NULL
+ * Returns SRWM_OK or an error code; x and y_out may be NULL only when T == 0.
+ */
+int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
+                 int softmax_input, float* y_out, float* W_final, void* stream);
+
+/*
+ * srwm_step -- one step of the same recurrence from a per-sequence state:
+ * W_out[b,h] = W_in[b,h] + update, y_t[b,h] = y from W_in[b,h].  Calling it T
+ * times, feeding W_out back as W_in, reproduces srwm_forward.
+ *
+ *   x_t    [B, H, d]      this step's inputs
+ *   W_in   [B, H, m, d]   current state of every stream (read)
+ *   y_t    [B, H, d]      written
+ *   W_out  [B, H, m, d]   written; may be the same pointer as W_in (in place)
+ *                         but must not partially overlap it
+ */
+int srwm_step(const float* x_t, const float* W_in, int B, int H, int d, int n_lr,
+              int softmax_input, float* y_t, float* W_out, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* srwm_status_string(int status);
+
+/*
+ * srwm_last_device_status -- synchronise `stream`, then read and clear the
+ * device status word that kernels set when a bounded wait gives up (a TMA
+ * transfer that never arrived).  Returns SRWM_OK, SRWM_ERR_TIMEOUT, or
+ * SRWM_ERR_CUDA if the synchronisation itself failed.
+ */
+int srwm_last_device_status(void* stream);
+
+/*
+ * srwm_set_wait_limit_ns -- the time after which a kernel's wait on an
+ * asynchronous copy gives up (default 1 s).  Values < 1000 are clamped to
+ * 1000.  Applies to launches made after the call, from any thread.
+ */
+int srwm_set_wait_limit_ns(long long limit_ns);
+
+/*
+ * srwm_debug_skip_x_chunk -- fault injection for tests: the next launches do
+ * not issue the TMA load of input chunk `chunk` (a chunk is a fixed number of
+ * consecutive steps) so the kernel's bounded wait on it runs out; -1 turns
+ * injection off.  The kernel then stops early, waits for its other copies,
+ * writes no further outputs, and sets the status word read by
+ * srwm_last_device_status.  Not for production use.
+ */
+int srwm_debug_skip_x_chunk(int chunk);
+
+/*
+ * srwm_probe_fma -- calibration kernel for the FP32 FMA roofline: `blocks` CTAs
+ * of `threads` threads each run `iters` iterations of 8 independent FMA chains
+ * (packed two-wide when `packed` is 1).  out[blocks*threads] receives the
+ * chains' sums (device memory).  One launch does blocks*threads*iters*8*(1+packed)
+ * FMAs; time it with CUDA events on `stream`.
+ */
+int srwm_probe_fma(int blocks, int threads, int iters, int packed, float* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SRWM_H */

@@ -1,0 +1,146 @@
+"""Python binding of libsrwm.so: argument marshalling only.
+
+Every step of the recurrence runs in the library's sm_103a kernels; this
+module checks tensor types, allocates outputs with torch when the caller does
+not pass them, and forwards raw device pointers and the current CUDA stream.
+If libsrwm.so is missing, every call raises: there is no fallback path.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libsrwm.so")
+_LIB = None
+
+# Status codes of include/srwm.h
+SRWM_OK = 0
+SRWM_ERR_TIMEOUT = 7
+
+EXPORTS = ("srwm_forward", "srwm_step", "srwm_status_string", "srwm_last_device_status",
+           "srwm_set_wait_limit_ns", "srwm_debug_skip_x_chunk", "srwm_probe_fma")
+
+
+class SrwmError(RuntimeError):
+    """A libsrwm call returned a non-zero status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {srwm_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is not built. Build it with "
+                "`python -m self_referential_weight_gb300.build` (needs nvcc).")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+        lib.srwm_forward.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
+        lib.srwm_forward.restype = I
+        lib.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
+        lib.srwm_step.restype = I
+        lib.srwm_status_string.argtypes = [I]
+        lib.srwm_status_string.restype = ctypes.c_char_p
+        lib.srwm_last_device_status.argtypes = [P]
+        lib.srwm_last_device_status.restype = I
+        lib.srwm_set_wait_limit_ns.argtypes = [LL]
+        lib.srwm_set_wait_limit_ns.restype = I
+        lib.srwm_debug_skip_x_chunk.argtypes = [I]
+        lib.srwm_debug_skip_x_chunk.restype = I
+        lib.srwm_probe_fma.argtypes = [I, I, I, I, P, P]
+        lib.srwm_probe_fma.restype = I
+        _LIB = lib
+    return _LIB
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t, name, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else 0)
+
+
+def _check(rc, where):
+    if rc != SRWM_OK:
+        raise SrwmError(rc, where)
+
+
+def srwm_status_string(status: int) -> str:
+    return _lib().srwm_status_string(int(status)).decode()
+
+
+def srwm_forward(x, W0, n_lr, softmax_input=False, y_out=None, W_final=None, stream=None):
+    """T steps of the SRWM recurrence for every (sequence, head) stream.
+
+    x [B,T,H,d] and W0 [H,m,d] (m = 3d + n_lr) are float32 CUDA tensors.
+    Returns (y [B,T,H,d], W_final [B,H,m,d]); outputs are allocated when not given.
+    """
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    if y_out is None:
+        y_out = torch.empty((B, T, H, d), dtype=torch.float32, device=x.device)
+    if W_final is None:
+        W_final = torch.empty((B, H, m, d), dtype=torch.float32, device=W0.device)
+    px = _dev(x, "x")
+    pw = _dev(W0, "W0", (H, m, d))
+    py = _dev(y_out, "y_out", (B, T, H, d))
+    pf = _dev(W_final, "W_final", (B, H, m, d))
+    rc = _lib().srwm_forward(px, pw, B, T, H, d, int(n_lr), int(bool(softmax_input)), py, pf,
+                             _stream_handle(stream))
+    _check(rc, "srwm_forward")
+    return y_out, W_final
+
+
+def srwm_step(x_t, W_in, n_lr, softmax_input=False, y_t=None, W_out=None, stream=None):
+    """One step from per-sequence states: x_t [B,H,d], W_in [B,H,m,d] -> (y_t, W_out).
+
+    W_out may be W_in itself (in-place update)."""
+    B, H, d = x_t.shape
+    m = 3 * d + n_lr
+    if y_t is None:
+        y_t = torch.empty((B, H, d), dtype=torch.float32, device=x_t.device)
+    if W_out is None:
+        W_out = torch.empty((B, H, m, d), dtype=torch.float32, device=W_in.device)
+    rc = _lib().srwm_step(_dev(x_t, "x_t"), _dev(W_in, "W_in", (B, H, m, d)), B, H, d, int(n_lr),
+                          int(bool(softmax_input)), _dev(y_t, "y_t", (B, H, d)),
+                          _dev(W_out, "W_out", (B, H, m, d)), _stream_handle(stream))
+    _check(rc, "srwm_step")
+    return y_t, W_out
+
+
+def srwm_last_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the kernels' status word."""
+    return _lib().srwm_last_device_status(_stream_handle(stream))
+
+
+def srwm_set_wait_limit_ns(limit_ns: int) -> None:
+    _check(_lib().srwm_set_wait_limit_ns(int(limit_ns)), "srwm_set_wait_limit_ns")
+
+
+def srwm_debug_skip_x_chunk(chunk: int) -> None:
+    _check(_lib().srwm_debug_skip_x_chunk(int(chunk)), "srwm_debug_skip_x_chunk")
+
+
+def srwm_probe_fma(blocks, threads, iters, packed, out, stream=None):
+    rc = _lib().srwm_probe_fma(int(blocks), int(threads), int(iters), int(bool(packed)),
+                               _dev(out, "out"), _stream_handle(stream))
+    _check(rc, "srwm_probe_fma")

@@ -1,0 +1,279 @@
+// srwm_api.cu -- the C ABI declared in include/srwm.h: argument checks, TMA
+// tensor maps, dispatch to the kernel instantiations, device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "srwm.h"
+#include "srwm_common.h"
+
+namespace {
+
+// Set by a kernel whose bounded wait ran out; read by srwm_last_device_status.
+__device__ unsigned int g_status_word;
+
+std::atomic<long long> g_wait_limit_ns{1000000000LL};
+std::atomic<int> g_skip_chunk{-1};
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+int status_ptr(unsigned** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        g_status_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return SRWM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Device memory of the current device (or managed memory)?
+int check_device_ptr(const void* p)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_NOT_DEVICE;
+    }
+    if (attr.type == cudaMemoryTypeManaged) return SRWM_OK;
+    if (attr.type != cudaMemoryTypeDevice) return SRWM_ERR_NOT_DEVICE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return attr.device == dev ? SRWM_OK : SRWM_ERR_NOT_DEVICE;
+}
+
+// 4-D map over a [B, T, H, d] fp32 tensor, dims innermost first {d, H, T, B};
+// one box is `tau` consecutive steps of one (b, h) stream: {d, 1, tau, 1}.
+int make_stream_map(CUtensorMap* map, const float* base, int B, int T, int H, int d, int tau)
+{
+    auto enc = encoder();
+    if (!enc) return SRWM_ERR_CUDA;
+    const cuuint64_t e = sizeof(float);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {e * d, e * d * H, e * d * H * static_cast<cuuint64_t>(T)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1u, static_cast<cuuint32_t>(tau), 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+srwm::LaunchInfo info_for(int d, int n_lr, int smx)
+{
+    if (d == 16) return srwm::launch_info_d16(n_lr, smx);
+    if (d == 32) return srwm::launch_info_d32(n_lr, smx);
+    return srwm::launch_info_d64(n_lr, smx);
+}
+
+int check_params(int B, int T, int H, int d, int n_lr, int softmax_input)
+{
+    if (B <= 0 || H <= 0 || d <= 0 || T < 0) return SRWM_ERR_SHAPE;
+    if (d != 16 && d != 32 && d != 64) return SRWM_ERR_UNSUPPORTED;
+    if (n_lr != 1 && n_lr != 4) return SRWM_ERR_UNSUPPORTED;
+    if (softmax_input != 0 && softmax_input != 1) return SRWM_ERR_UNSUPPORTED;
+    // Every element count must fit the int64 byte arithmetic below and every
+    // TMA stride must stay below 2^40 bytes.
+    const long long m = 3LL * d + n_lr;
+    const long long pairs = static_cast<long long>(B) * H;
+    if (pairs > (1LL << 31) - 1) return SRWM_ERR_SHAPE;
+    const long long step_bytes = static_cast<long long>(H) * d * 4;
+    if (step_bytes * static_cast<long long>(T > 0 ? T : 1) >= (1LL << 40)) return SRWM_ERR_SHAPE;
+    if (pairs * m * d > (1LL << 60) / 4) return SRWM_ERR_SHAPE;
+    return SRWM_OK;
+}
+
+int launch(const srwm::LaunchInfo& li, const CUtensorMap& tx, const CUtensorMap& ty,
+           const srwm::KParams& kp, long long pairs, cudaStream_t stream)
+{
+    if (li.smem_bytes > 48 * 1024) {
+        if (cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 li.smem_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(srwm::cdiv(static_cast<int>(pairs), li.streams_per_cta)));
+    const dim3 block(static_cast<unsigned>(li.threads));
+    void* args[] = {const_cast<CUtensorMap*>(&tx), const_cast<CUtensorMap*>(&ty),
+                    const_cast<srwm::KParams*>(&kp)};
+    if (cudaLaunchKernel(li.kernel, grid, block, args, static_cast<size_t>(li.smem_bytes), stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return SRWM_OK;
+}
+
+// Shared body of srwm_forward (per_seq = 0) and srwm_step (per_seq = 1, T = 1).
+int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, int d, int n_lr,
+        int smx, float* y, float* W_out, cudaStream_t stream)
+{
+    const long long m = 3LL * d + n_lr;
+    const size_t nx = static_cast<size_t>(B) * T * H * d * sizeof(float);
+    const size_t nw_in = static_cast<size_t>(per_seq ? B : 1) * H * m * d * sizeof(float);
+    const size_t nw_out = static_cast<size_t>(B) * H * m * d * sizeof(float);
+
+    if (!aligned16(W_init) || !aligned16(W_out) || (T > 0 && (!aligned16(x) || !aligned16(y))))
+        return SRWM_ERR_ALIGN;
+    if (T > 0) {
+        if (overlaps(y, nx, x, nx) || overlaps(y, nx, W_init, nw_in) || overlaps(y, nx, W_out, nw_out))
+            return SRWM_ERR_ALIAS;
+        if (overlaps(W_out, nw_out, x, nx)) return SRWM_ERR_ALIAS;
+    }
+    if (overlaps(W_out, nw_out, W_init, nw_in) && !(per_seq && W_out == W_init)) return SRWM_ERR_ALIAS;
+
+    int rc;
+    if ((rc = check_device_ptr(W_init)) != SRWM_OK) return rc;
+    if ((rc = check_device_ptr(W_out)) != SRWM_OK) return rc;
+    if (T > 0) {
+        if ((rc = check_device_ptr(x)) != SRWM_OK) return rc;
+        if ((rc = check_device_ptr(y)) != SRWM_OK) return rc;
+    }
+
+    const srwm::LaunchInfo li = info_for(d, n_lr, smx);
+    CUtensorMap tx, ty;
+    std::memset(&tx, 0, sizeof(tx));
+    std::memset(&ty, 0, sizeof(ty));
+    if (T > 0) {
+        if ((rc = make_stream_map(&tx, x, B, T, H, d, li.tau)) != SRWM_OK) return rc;
+        if ((rc = make_stream_map(&ty, y, B, T, H, d, li.tau)) != SRWM_OK) return rc;
+    }
+    srwm::KParams kp;
+    kp.W_init = W_init;
+    kp.W_out = W_out;
+    if ((rc = status_ptr(&kp.status)) != SRWM_OK) return rc;
+    kp.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+    kp.B = B;
+    kp.T = T;
+    kp.H = H;
+    kp.w_per_seq = per_seq;
+    kp.skip_chunk = g_skip_chunk.load();
+    return launch(li, tx, ty, kp, static_cast<long long>(B) * H, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
+                 int softmax_input, float* y_out, float* W_final, void* stream)
+{
+    if (!W0 || !W_final || (T > 0 && (!x || !y_out))) return SRWM_ERR_NULL;
+    const int rc = check_params(B, T, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    return run(x, W0, 0, B, T, H, d, n_lr, softmax_input, y_out, W_final,
+               static_cast<cudaStream_t>(stream));
+}
+
+int srwm_step(const float* x_t, const float* W_in, int B, int H, int d, int n_lr,
+              int softmax_input, float* y_t, float* W_out, void* stream)
+{
+    if (!x_t || !W_in || !y_t || !W_out) return SRWM_ERR_NULL;
+    const int rc = check_params(B, 1, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    return run(x_t, W_in, 1, B, 1, H, d, n_lr, softmax_input, y_t, W_out,
+               static_cast<cudaStream_t>(stream));
+}
+
+const char* srwm_status_string(int status)
+{
+    switch (status) {
+        case SRWM_OK: return "SRWM_OK";
+        case SRWM_ERR_NULL: return "SRWM_ERR_NULL: a required pointer is NULL";
+        case SRWM_ERR_SHAPE: return "SRWM_ERR_SHAPE: invalid or too large B/T/H/d";
+        case SRWM_ERR_UNSUPPORTED: return "SRWM_ERR_UNSUPPORTED: d must be 16/32/64, n_lr 1/4, softmax_input 0/1";
+        case SRWM_ERR_ALIGN: return "SRWM_ERR_ALIGN: pointers must be 16-byte aligned";
+        case SRWM_ERR_ALIAS: return "SRWM_ERR_ALIAS: an output overlaps an input or another output";
+        case SRWM_ERR_CUDA: return "SRWM_ERR_CUDA: a CUDA runtime call failed";
+        case SRWM_ERR_TIMEOUT: return "SRWM_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        case SRWM_ERR_NOT_DEVICE: return "SRWM_ERR_NOT_DEVICE: pointer is not device memory of the current device";
+        default: return "SRWM: unknown status";
+    }
+}
+
+int srwm_last_device_status(void* stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    unsigned* dptr = nullptr;
+    int rc = status_ptr(&dptr);
+    if (rc != SRWM_OK) return rc;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, dptr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    if (v == 0) return SRWM_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpy(dptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return (v & srwm::kStatusTimeout) ? SRWM_ERR_TIMEOUT : SRWM_ERR_CUDA;
+}
+
+int srwm_set_wait_limit_ns(long long limit_ns)
+{
+    g_wait_limit_ns.store(limit_ns < 1000 ? 1000 : limit_ns);
+    return SRWM_OK;
+}
+
+int srwm_debug_skip_x_chunk(int chunk)
+{
+    g_skip_chunk.store(chunk < 0 ? -1 : chunk);
+    return SRWM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// srwm_common.h -- definitions shared by the kernels and the host-side C ABI.
+#pragma once
+
+#if defined(__CUDACC__)
+#define SRWM_HD __host__ __device__
+#else
+#define SRWM_HD
+#endif
+
+namespace srwm {
+
+SRWM_HD constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
+SRWM_HD constexpr int rup(int a, int b) { return cdiv(a, b) * b; }
+
+// Bits of the device status word.
+constexpr unsigned kStatusTimeout = 1u;
+
+// Kernel arguments besides the two tensor maps.
+struct KParams {
+    const float* W_init;               // [H,m,d] shared, or [B,H,m,d] per sequence
+    float* W_out;                      // [B,H,m,d]
+    unsigned* status;                  // device status word
+    unsigned long long wait_limit_ns;  // bounded-wait limit
+    int B, T, H;
+    int w_per_seq;                     // 1: W_init is per sequence
+    int skip_chunk;                    // fault injection: x chunk not loaded (-1: none)
+};
+
+// What the host needs to launch one template instantiation.
+struct LaunchInfo {
+    const void* kernel;   // __global__ function
+    int threads;          // per CTA
+    int streams_per_cta;  // (sequence, head) streams per CTA
+    int smem_bytes;       // dynamic shared memory
+    int tau;              // steps per TMA chunk (box height of the x / y tensor maps)
+};
+
+LaunchInfo launch_info_d16(int n_lr, int softmax_input);
+LaunchInfo launch_info_d32(int n_lr, int softmax_input);
+LaunchInfo launch_info_d64(int n_lr, int softmax_input);
+
+}  // namespace srwm

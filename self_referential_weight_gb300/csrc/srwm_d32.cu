@@ -1,0 +1,13 @@
+// srwm_d32.cu -- instantiations of the d = 32 kernels (one translation unit
+// per width so the library builds in parallel).
+#include "srwm_kernels.cuh"
+
+namespace srwm {
+
+LaunchInfo launch_info_d32(int n_lr, int softmax_input)
+{
+    if (n_lr == 1) return softmax_input ? launch_info<32, 1, true>() : launch_info<32, 1, false>();
+    return softmax_input ? launch_info<32, 4, true>() : launch_info<32, 4, false>();
+}
+
+}  // namespace srwm

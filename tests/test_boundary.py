@@ -1,0 +1,108 @@
+"""Host-only checks of the C ABI (no GPU needed): the library builds, exports
+every entry point declared in include/srwm.h, and rejects bad arguments before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from self_referential_weight_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "srwm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = lib_build.build()
+    L = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.srwm_forward.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
+    L.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
+    L.srwm_status_string.restype = ctypes.c_char_p
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(srwm_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("srwm_forward", "srwm_step", "srwm_status_string", "srwm_last_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_lists_the_same_exports():
+    from self_referential_weight_gb300 import binding
+    assert sorted(binding.EXPORTS) == declared_functions()
+
+
+A = 0x100000  # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def fwd(lib, x=A, W0=A + 0x1000000, B=2, T=3, H=2, d=16, n_lr=4, smx=0, y=A + 0x2000000,
+        Wf=A + 0x3000000):
+    return lib.srwm_forward(x, W0, B, T, H, d, n_lr, smx, y, Wf, None)
+
+
+def test_null_pointers(lib):
+    assert fwd(lib, x=None) == 1
+    assert fwd(lib, W0=None) == 1
+    assert fwd(lib, y=None) == 1
+    assert fwd(lib, Wf=None) == 1
+    assert lib.srwm_step(None, A, 1, 1, 16, 4, 0, A, A, None) == 1
+
+
+def test_bad_shapes(lib):
+    assert fwd(lib, B=0) == 2
+    assert fwd(lib, H=-1) == 2
+    assert fwd(lib, T=-1) == 2
+    assert fwd(lib, d=0) == 2
+    assert fwd(lib, B=1 << 20, H=1 << 12) == 2  # more than 2^31 streams
+
+
+def test_unsupported(lib):
+    assert fwd(lib, d=48) == 3
+    assert fwd(lib, d=128) == 3
+    assert fwd(lib, n_lr=2) == 3
+    assert fwd(lib, smx=2) == 3
+
+
+def test_alignment(lib):
+    assert fwd(lib, x=A + 4) == 4
+    assert fwd(lib, Wf=A + 0x3000008) == 4
+
+
+def test_aliasing(lib):
+    # y overlapping x, W_final overlapping y
+    assert fwd(lib, y=A) == 5
+    assert fwd(lib, Wf=A + 0x2000000 + 64) == 5
+    # step: exact in-place W is allowed past the alias check, partial overlap is not
+    assert lib.srwm_step(A, A + 0x1000000, 1, 1, 16, 4, 0, A + 0x2000000, A + 0x1000000 + 16, None) == 5
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.srwm_status_string(code).decode()
+        assert s.startswith("SRWM")
+    assert "unknown" in lib.srwm_status_string(99).decode()
+
+
+def test_oracle_library_is_separate():
+    """The oracle is its own library; the CUDA library exports none of its symbols."""
+    import oracle
+    from oracle import build as ob
+    ob.build()
+    names = set(re.findall(r"\b(srwm_oracle_\w+)", open(os.path.join(ROOT, "oracle", "srwm_oracle.c")).read()))
+    lib = ctypes.CDLL(lib_build.LIB)
+    for n in names:
+        assert not hasattr(lib, n)
+    assert oracle.lib_path() != lib_build.LIB

@@ -1,0 +1,44 @@
+"""Bounded waits: a TMA load that never arrives ends the kernel with a status,
+not a hang, and leaves the context usable.
+
+The fault is made on the host: srwm_debug_skip_x_chunk(1) makes the kernels
+skip issuing the load of input chunk 1, so the wait for it runs out after the
+(shortened) wait limit.  Nothing faults or traps on the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from self_referential_weight_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture
+def short_waits():
+    binding.srwm_set_wait_limit_ns(50_000_000)  # 50 ms
+    yield
+    binding.srwm_debug_skip_x_chunk(-1)
+    binding.srwm_set_wait_limit_ns(1_000_000_000)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_missing_chunk_times_out_then_recovers(short_waits, d):
+    wl = inputs.Workload("t", 2, 100, 3, d, 4, False, 40 + d, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
+    assert binding.srwm_last_device_status() == 0
+
+    binding.srwm_debug_skip_x_chunk(1)
+    binding.srwm_forward(xd, W0d, 4)
+    assert binding.srwm_last_device_status() == binding.SRWM_ERR_TIMEOUT
+    assert binding.srwm_last_device_status() == 0  # reading clears it
+
+    binding.srwm_debug_skip_x_chunk(-1)
+    y, Wf = binding.srwm_forward(xd, W0d, 4)
+    assert binding.srwm_last_device_status() == 0
+    yo, Wo = oracle.forward(x, W0, 4)
+    assert np.abs(y.cpu().numpy() - yo).max() / np.abs(yo).max() <= 1e-4
+    assert np.abs(Wf.cpu().numpy() - Wo).max() / np.abs(Wo).max() <= 1e-4

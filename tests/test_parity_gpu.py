@@ -1,0 +1,205 @@
+"""GPU parity: the sm_103a library against the CPU oracle, element by element,
+on the same seeded inputs.
+
+Tolerance (fp32 state and arithmetic against the float64 oracle):
+    max|gpu - oracle| / max|oracle| <= 1e-4 for T <= 1024, <= 1e-3 up to T = 8192,
+for y and for W_final alike.  The oracle's own fp32 floor on these workloads is
+<= 5e-6 (tests/test_oracle_pins.py::test_c8_fp32_floor).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from self_referential_weight_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def tol(T):
+    return 1e-4 if T <= 1024 else 1e-3
+
+
+def rel(a, b):
+    return float(np.abs(np.asarray(a, np.float64) - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def run_gpu(x, W0, n_lr, smx):
+    y, Wf = binding.srwm_forward(torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV), n_lr, smx)
+    torch.cuda.synchronize()
+    assert binding.srwm_last_device_status() == 0
+    return y.cpu().numpy(), Wf.cpu().numpy()
+
+
+# ------------------------------------------------------------------ small shapes
+# Several TMA chunks (16 steps for d <= 32, 32 for d = 64) plus a ragged tail,
+# and stream counts that leave the last CTA partly empty.
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("n_lr", [1, 4])
+@pytest.mark.parametrize("smx", [False, True])
+def test_small_all_variants(d, n_lr, smx):
+    wl = inputs.Workload("t", 3, 75, 3, d, n_lr, smx, 10 + d + n_lr + smx, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    assert rel(y, yo) <= 1e-4
+    assert rel(Wf, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 31, 32, 33, 64])
+def test_step_count_edges(d, T):
+    wl = inputs.Workload("t", 2, T, 5, d, 4, False, 100 + T, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, 4, False)
+    yo, Wo = oracle.forward(x, W0, 4, False)
+    assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_zero_steps_copies_W0(d):
+    W0 = inputs.make_W0(3, d, 4, seed=5)
+    x = torch.empty((2, 0, 3, d), device=DEV)
+    y, Wf = binding.srwm_forward(x, torch.from_numpy(W0).to(DEV), 4)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(Wf.cpu().numpy(), np.broadcast_to(W0, (2,) + W0.shape))
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_zero_matrix_stays_zero(d):
+    """The W0 = 0 fixed point holds exactly on the GPU too."""
+    wl = inputs.Workload("t", 2, 40, 2, d, 4, False, 7, "normal")
+    x = inputs.make_x(wl)
+    W0 = np.zeros((2, 3 * d + 4, d), np.float32)
+    y, Wf = run_gpu(x, W0, 4, False)
+    assert not y.any() and not Wf.any()
+
+
+@pytest.mark.parametrize("n_streams", [1, 5, 6, 7, 8, 9, 13, 17])
+def test_stream_counts_fill_ctas(n_streams):
+    """Streams per CTA are 8 (d=16) and 6 (d=32): counts around those."""
+    for d in (16, 32):
+        wl = inputs.Workload("t", n_streams, 20, 1, d, 4, False, n_streams, "normal")
+        x, W0 = inputs.make_inputs(wl)
+        y, Wf = run_gpu(x, W0, 4, False)
+        yo, Wo = oracle.forward(x, W0, 4, False)
+        assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
+
+
+# ------------------------------------------------------------------ named workloads
+def test_tiny_full():
+    wl = inputs.workload("tiny")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, wl.n_lr, wl.softmax_input)
+    yo, Wo = oracle.forward(x, W0, wl.n_lr, wl.softmax_input)
+    assert rel(y, yo) <= tol(wl.T) and rel(Wf, Wo) <= tol(wl.T)
+
+
+def test_fewshot_full():
+    wl = inputs.workload("fewshot")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, wl.n_lr, wl.softmax_input)
+    yo, Wo = oracle.forward(x, W0, wl.n_lr, wl.softmax_input)
+    assert rel(y, yo) <= tol(wl.T) and rel(Wf, Wo) <= tol(wl.T)
+
+
+@pytest.mark.parametrize("name", ["mid", "long", "rl"])
+def test_full_size_sampled_streams(name):
+    """Full-size launch (the benchmark's configuration); the oracle recomputes a
+    sample of (b, h) streams one by one, covering the first and last CTAs."""
+    wl = inputs.workload(name)
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, wl.n_lr, wl.softmax_input)
+    rng = np.random.default_rng(0)
+    picks = {(0, 0), (wl.B - 1, wl.H - 1)}
+    while len(picks) < 8:
+        picks.add((int(rng.integers(wl.B)), int(rng.integers(wl.H))))
+    for b, h in sorted(picks):
+        yo, Wo = oracle.forward(x[b:b + 1, :, h:h + 1], W0[h:h + 1], wl.n_lr, wl.softmax_input)
+        ey, ew = rel(y[b, :, h], yo[0, :, 0]), rel(Wf[b, h], Wo[0, 0])
+        assert ey <= tol(wl.T) and ew <= tol(wl.T), (b, h, ey, ew)
+
+
+# ------------------------------------------------------------------ structure
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_stream_slice_is_bitwise_equal(d):
+    """Streams are independent: running one (b, h) alone gives the same bits."""
+    wl = inputs.Workload("t", 3, 50, 4, d, 4, False, 21, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, 4, False)
+    for b, h in [(0, 0), (2, 3), (1, 2)]:
+        ys, Wfs = run_gpu(np.ascontiguousarray(x[b:b + 1, :, h:h + 1]), W0[h:h + 1], 4, False)
+        np.testing.assert_array_equal(ys[0, :, 0], y[b, :, h])
+        np.testing.assert_array_equal(Wfs[0, 0], Wf[b, h])
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_deterministic(d):
+    wl = inputs.Workload("t", 4, 70, 3, d, 1, True, 22, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    a = run_gpu(x, W0, 1, True)
+    b = run_gpu(x, W0, 1, True)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
+def test_step_matches_oracle_and_chains_to_forward(d, n_lr, smx):
+    """srwm_step from per-sequence states equals the oracle's one step; T
+    chained steps (in place) equal one srwm_forward call."""
+    wl = inputs.Workload("t", 3, 12, 2, d, n_lr, smx, 30 + d, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    m = wl.m
+    # one step from distinct per-sequence states
+    Wseq = (W0[None] + 0.05 * np.random.default_rng(1).standard_normal((3, 2, m, d))).astype(np.float32)
+    yt, Wo = binding.srwm_step(torch.from_numpy(np.ascontiguousarray(x[:, 0])).to(DEV),
+                               torch.from_numpy(Wseq).to(DEV), n_lr, smx)
+    torch.cuda.synchronize()
+    yo, Woo = oracle.forward(x[:, :1], Wseq, n_lr, smx, per_sequence=True)
+    assert rel(yt.cpu().numpy(), yo[:, 0]) <= 1e-5
+    assert rel(Wo.cpu().numpy(), Woo) <= 1e-5
+    # chained in place
+    W = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(W0, (3, 2, m, d)))).to(DEV)
+    ys = []
+    for t in range(wl.T):
+        yt, _ = binding.srwm_step(torch.from_numpy(np.ascontiguousarray(x[:, t])).to(DEV), W, n_lr, smx,
+                                  W_out=W)
+        ys.append(yt.cpu().numpy())
+    y_chain = np.stack(ys, axis=1)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    assert rel(y_chain, y) <= 1e-5
+    assert rel(W.cpu().numpy(), Wf) <= 1e-5
+
+
+# ------------------------------------------------------------------ boundary on a GPU
+def test_host_pointer_is_rejected():
+    lib = binding._lib()
+    x = torch.zeros((1, 4, 1, 16))           # host memory
+    W0 = torch.zeros((1, 52, 16), device=DEV)
+    y = torch.zeros((1, 4, 1, 16), device=DEV)
+    Wf = torch.zeros((1, 1, 52, 16), device=DEV)
+    rc = lib.srwm_forward(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(W0.data_ptr()), 1, 4, 1, 16,
+                          4, 0, ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(Wf.data_ptr()), None)
+    assert rc == 8
+
+
+def test_device_alias_is_rejected():
+    buf = torch.zeros(4096, device=DEV)
+    lib = binding._lib()
+    p = buf.data_ptr()
+    rc = lib.srwm_forward(ctypes.c_void_p(p), ctypes.c_void_p(p + 8192), 1, 4, 1, 16, 4, 0,
+                          ctypes.c_void_p(p + 64), ctypes.c_void_p(p + 12288), None)
+    assert rc == 5
+
+
+def test_binding_raises_on_error():
+    x = torch.zeros((1, 4, 1, 48), device=DEV)
+    W0 = torch.zeros((1, 148, 48), device=DEV)
+    with pytest.raises(binding.SrwmError) as e:
+        binding.srwm_forward(x, W0, 4)
+    assert e.value.status == 3
