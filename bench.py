@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the SRWM forward recurrence on GB300.
+
+One step = one srwm_forward call over the whole workload (every row of the hot
+path: input softmax when enabled, Eq. (1) read-out, phi of k and q, gates,
+fused Eq. (2)/(3) update).  Default workload: "mid" (B=64, T=1024, H=8, d=64,
+four learning rates), the d = 64 configuration the FP32-FMA target is stated
+for, one GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+copy of the workload on its own GPU (weak scaling, no data-path collective);
+value = all ranks' head-tokens / max-over-ranks time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from self_referential_weight_gb300 import inputs  # noqa: E402
+
+METRIC = "SRWM head-token updates/s (B*T*H/s) and % of FP32 FMA peak, 1 GB300"
+UNIT = "head-token updates/s"
+FMA_PER_CLK_PER_SM = 128          # FP32 FMA lanes per SM (4 SMSPs x 32)
+L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "srwm_cta_kernel_mid.md")
+KERNEL_SOURCES = ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mid", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def fmas_per_head_token(wl):
+    return 3 * wl.m * wl.d
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "self_referential_weight_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload with the current kernel sources; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    wl = re.search(r"workload:\s*(\w+)", text)
+    tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (src and wl and tr) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
+        return None
+    return int(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(wl, x, W0, target_s=10.0):
+    """The float64 oracle, as it stands, on this host's cores, on a bounded sample
+    of the workload's (b, h) streams at full T.  Returns the JSON object."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    # calibrate on a handful of streams, then size the sample to ~target_s
+    n_cal = min(wl.B * wl.H, max(cores, 8))
+    pairs = [(i // wl.H, i % wl.H) for i in range(wl.B * wl.H)]
+
+    def run(n):
+        sel = pairs[:n]
+        xs = np.ascontiguousarray(np.stack([x[b, :, h] for b, h in sel], axis=0)[:, :, None, :])
+        Ws = np.ascontiguousarray(np.stack([W0[h] for _, h in sel], axis=0)[:, None])
+        t0 = time.perf_counter()
+        oracle.forward(xs, Ws, wl.n_lr, wl.softmax_input, per_sequence=True, n_threads=cores)
+        return time.perf_counter() - t0
+
+    t_cal = run(n_cal)
+    n = int(min(wl.B * wl.H, max(n_cal, n_cal * target_s / max(t_cal, 1e-6))))
+    n = max(cores, (n // cores) * cores) if n >= cores else n
+    n = min(n, wl.B * wl.H)
+    dt = run(n)
+    return {"value": n * wl.T / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {wl.B * wl.H} (b,h) streams x {wl.T} steps of the {wl.name} "
+                      f"workload, float64 C oracle, one pthread per core over streams",
+            "seconds": dt}
+
+
+def reference_arm(args, wl):
+    """--impl reference: the oracle timed on the host cores, each step a bounded
+    sample of the workload."""
+    import oracle
+
+    x, W0 = inputs.make_inputs(wl)
+    cores = os.cpu_count() or 1
+    n = min(wl.B * wl.H, 2 * cores)
+    sel = [(i // wl.H, i % wl.H) for i in range(n)]
+    xs = np.ascontiguousarray(np.stack([x[b, :, h] for b, h in sel], axis=0)[:, :, None, :])
+    Ws = np.ascontiguousarray(np.stack([W0[h] for _, h in sel], axis=0)[:, None])
+
+    def step():
+        oracle.forward(xs, Ws, wl.n_lr, wl.softmax_input, per_sequence=True, n_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = n * wl.T * args.steps / tot
+    sample = (f"{n} of {wl.B * wl.H} (b,h) streams x {wl.T} steps of the {wl.name} workload per "
+              f"step, float64 C oracle, {cores} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d": wl.d, "m": wl.m,
+            "n_lr": wl.n_lr, "softmax_input": wl.softmax_input,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "inputs": "seeded SplitMix64/Box-Muller synthetic, x ~ N(0,1), W0 ~ N(0,1/d)"}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    wl = inputs.workload(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, wl)
+        return
+
+    import torch
+
+    from self_referential_weight_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # per-rank data: the same workload shape, a rank-specific seed (weak scaling)
+    wl_r = wl.with_shape(seed=wl.seed + 1000 * rank) if rank else wl
+    x_np, W0_np = inputs.make_inputs(wl_r)
+    x = torch.from_numpy(x_np).to(dev)
+    W0 = torch.from_numpy(W0_np).to(dev)
+    y = torch.empty_like(x)
+    Wf = torch.empty((wl.B, wl.H, wl.m, wl.d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.srwm_forward(x, W0, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if binding.srwm_last_device_status(stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---------------- device-timed region: K steps, L2 flushed between steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with (clocks if not args.no_clocks else _Null()):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    t_dev = sum(per_step) / 1e3
+    if binding.srwm_last_device_status(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+    t_max = t_dev
+    if world > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([t_dev], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+
+    ht_per_step = wl.head_tokens
+    value = world * ht_per_step * args.steps / t_max
+    ms_per_step = 1e3 * t_max / args.steps
+
+    # ---------------- end to end through the public API with host buffers
+    x_h = torch.from_numpy(x_np).pin_memory()
+    W0_h = torch.from_numpy(W0_np).pin_memory()
+    y_h = torch.empty(x_h.shape, dtype=torch.float32).pin_memory()
+    Wf_h = torch.empty(tuple(Wf.shape), dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(x)
+    W0d = torch.empty_like(W0)
+
+    def e2e_step():
+        xd.copy_(x_h, non_blocking=True)
+        W0d.copy_(W0_h, non_blocking=True)
+        binding.srwm_forward(xd, W0d, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        Wf_h.copy_(Wf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": world * ht_per_step * args.e2e_steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": x_h.numel() * 4 + W0_h.numel() * 4,
+           "d2h_bytes_per_step": y_h.numel() * 4 + Wf_h.numel() * 4,
+           "ms_per_step": 1e3 * t_e2e / args.e2e_steps}
+    # the e2e outputs are the device outputs
+    if not torch.equal(y_h, y.cpu()):
+        raise RuntimeError("e2e copy-back mismatch")
+
+    # ---------------- FMA probe (calibration of the FP32 roofline)
+    props = torch.cuda.get_device_properties(dev)
+    n_sm = props.multi_processor_count
+    probe = fma_probe(binding, n_sm, stream)
+
+    if rank != 0:
+        return
+    clk = clocks.summary() if not args.no_clocks else {"sm_mhz": None, "sm_max_mhz": None,
+                                                        "reasons": ["unsampled"], "samples": 0}
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    f_max_mhz = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
+    peak_tflops = n_sm * FMA_PER_CLK_PER_SM * 2 * f_max_mhz * 1e6 / 1e12
+    flops_per_launch = 2.0 * fmas_per_head_token(wl) * ht_per_step
+    kernel_s = statistics.fmean(per_step) / 1e3
+    achieved = flops_per_launch / kernel_s / 1e12
+    peak_load = (n_sm * FMA_PER_CLK_PER_SM * 2 * clk["sm_mhz"] * 1e6 / 1e12) if clk["sm_mhz"] else None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "fma_peak_frac": achieved / peak_tflops,
+        "roofline": {
+            "bound": "alu",
+            "achieved": achieved,
+            "peak": peak_tflops,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak_tflops,
+            "traffic": profiled_traffic(wl.name),
+            "kernel": "srwm_cta_kernel" if wl.d == 64 else "srwm_warp_kernel",
+            "flops_per_launch": flops_per_launch,
+            "peak_basis": f"{n_sm} SMs x {FMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 flop x "
+                          f"{f_max_mhz:.0f} MHz (max SM clock)",
+            "frac_at_load_clock": (achieved / peak_load) if peak_load else None,
+        },
+        "fma_probe": probe,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                   "reasons": clk["reasons"], "samples": clk["samples"]},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": t_wall,
+        "ms_per_step_best": min(per_step),
+        "ms_per_step_median": statistics.median(per_step),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, x_np, W0_np)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def fma_probe(binding, n_sm, stream):
+    """FP32 FMA throughput of the calibration kernel (scalar and two-wide)."""
+    import torch
+
+    threads, iters = 512, 4096
+    blocks = n_sm * 4
+    out = torch.empty(blocks * threads, dtype=torch.float32, device="cuda")
+    res = {}
+    for packed in (0, 1):
+        binding.srwm_probe_fma(blocks, threads, iters, packed, out, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        reps = 5
+        for _ in range(reps):
+            binding.srwm_probe_fma(blocks, threads, iters, packed, out, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        s = e0.elapsed_time(e1) / 1e3 / reps
+        fmas = blocks * threads * iters * 8 * (2 if packed else 1)
+        res["tflops_packed" if packed else "tflops_scalar"] = 2 * fmas / s / 1e12
+    return res
+
+
+if __name__ == "__main__":
+    main()
