@@ -1,0 +1,427 @@
+// srwm_d64.cuh -- the d = 64 kernel: one (sequence, head) stream per CTA of
+// four warps, two CTAs per SM.
+//
+// Math (per step t; "Metalearning Continual Learning Algorithms", section 2.3,
+// Eqs. (1)-(3), four-rate version Eqs. (4)-(5)):
+//   phi_k = softmax(k_t), phi_q = softmax(q_t), g = sigmoid(beta_t) per block
+//   a_r   = W_{t-1}[r,:] . (phi_q - phi_k)                 (Eq. (2), both reads fused)
+//   W_t[r,:] = W_{t-1}[r,:] + g_r a_r phi_k                 (Eq. (3) / (5))
+//   z_{t+1,r} = W_t[r,:] . x~_{t+1} = b_r + g_r a_r (phi_k . x~_{t+1}),
+//               b_r = W_{t-1}[r,:] . x~_{t+1}               (Eq. (1) of step t+1)
+// so y_{t+1} = z_{t+1}[0:64] is still read from the pre-update matrix of its
+// own step (W_t).
+//
+// Layout.  Thread (rg = tid/4, cg = tid%4) holds rows rg + 32 i (i = 0..5:
+// blocks y, y, k, k, q, q) and, in warp 0, row 192 + rg (beta rows, valid for
+// rg < n_lr), over the 16 columns of float4 chunks cg, cg+4, cg+8, cg+12, kept
+// as float2 pairs for the two-wide FMA.  W never leaves registers.
+//
+// One step, one CTA barrier:
+//   1. every warp computes phi_k, phi_q and the gates from z_t in shared
+//      memory (redux max, exp, fixed-point redux sum, approximate reciprocal);
+//      meanwhile it applies the previous step's rank-one update fused with the
+//      dot products b_r against x~_{t+1};
+//   2. phi_k / phi_q go through a warp-private shared buffer into the thread's
+//      column layout; a_r and the partial phi_k . x~_{t+1};
+//   3. two xor-shuffle levels finish the dots; owner lanes store z_{t+1}
+//      (y rows to the TMA staging buffer, k/q/beta rows to shared memory);
+//   4. barrier.
+// The update of step t is applied at the start of step t+1 (or after the
+// loop), so it overlaps the softmax latency instead of preceding the barrier.
+// z is double-buffered by step parity (a fast warp writes z_{t+1} while a slow
+// one still reads z_t); y staging is triple-buffered (one chunk being written,
+// up to two still read by bulk stores).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "srwm_common.h"
+#include "srwm_ptx.cuh"
+
+namespace srwm {
+
+namespace d64 {
+
+constexpr int D = 64;
+constexpr int NT = 128;     // threads per CTA (one stream)
+constexpr int SLOTS = 6;    // row slots of every thread (rows 0..191)
+constexpr int TAU = 32;     // steps per TMA chunk
+constexpr int NP = 8;       // float2 column pairs per thread
+constexpr int XW = 3;       // warp staging x~ and driving the x TMA ring
+
+struct __align__(128) Smem {
+    float xring[2][TAU][D];    // TMA destination: raw x, two chunks
+    float ystage[3][TAU][D];   // TMA source: y, three chunks
+    float z[2][D * 3 + 8];     // k, q, beta rows of z_t by step parity (index = row)
+    float xs[2][D];            // x~_{t+1}, x~_{t+2}
+    float pkq[4][2][D];        // per warp: phi_k, phi_q in plain column order
+    uint64_t xbar[2];          // "chunk landed" barriers of the x ring
+};
+
+__device__ __forceinline__ float redux_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t redux_add(uint32_t v)
+{
+    uint32_t r;
+    asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float v)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Warp sum of two values in [0, 1] per lane, exact in fixed point with 2^-31
+// resolution (16-bit halves keep the u32 sums from overflowing).  Every lane
+// gets the same bits whatever the order of lanes.
+__device__ __forceinline__ float warp_sum_unit(float e0, float e1)
+{
+    const uint32_t q0 = __float2uint_rn(e0 * 2147483648.0f);
+    const uint32_t q1 = __float2uint_rn(e1 * 2147483648.0f);
+    const uint32_t hi = redux_add((q0 >> 16) + (q1 >> 16));
+    const uint32_t lo = redux_add((q0 & 0xffffu) + (q1 & 0xffffu));
+    return fmaf(static_cast<float>(hi), 3.0517578125e-05f, static_cast<float>(lo) * 4.656612873077393e-10f);
+}
+
+// softmax over 64 values held as (v0, v1) = entries (lane, lane + 32).
+__device__ __forceinline__ void softmax64(float v0, float v1, float& p0, float& p1)
+{
+    const float mx = redux_max(fmaxf(v0, v1));
+    const float e0 = __expf(v0 - mx), e1 = __expf(v1 - mx);
+    const float inv = rcp_approx(warp_sum_unit(e0, e1));
+    p0 = e0 * inv;
+    p1 = e1 * inv;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.0f + __expf(-v)); }
+
+__device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&out)[NP])
+{
+#pragma unroll
+    for (int j = 0; j < NP / 2; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(base + 4 * (cg + 4 * j));
+        out[2 * j] = make_float2(v.x, v.y);
+        out[2 * j + 1] = make_float2(v.z, v.w);
+    }
+}
+
+}  // namespace d64
+
+template <int NLR, bool SMX>
+__global__ void __launch_bounds__(d64::NT, 2)
+    srwm_d64_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+                    const KParams kp)
+{
+    using namespace d64;
+    constexpr int M = 3 * D + NLR;
+    constexpr int S1 = SLOTS + 1;
+    extern __shared__ unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rg = tid >> 2, cg = tid & 3;
+    const bool has_beta = (warp == 0);   // warp-uniform: slot 6 = row 192 + rg
+    const int p = blockIdx.x;
+    const int b = p / kp.H, h = p - b * kp.H;
+    const int T = kp.T;
+    const int nchunks = cdiv(T, TAU);
+
+    // ---- W -> registers
+    float2 w[S1][NP];
+    {
+        const float* Ws = kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * M * D;
+#pragma unroll
+        for (int i = 0; i < S1; ++i) {
+            const int r = (i < SLOTS) ? rg + 32 * i : 3 * D + rg;
+            const bool ok = (i < SLOTS) || (has_beta && r < M);
+#pragma unroll
+            for (int j = 0; j < NP / 2; ++j) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ok) v = __ldg(reinterpret_cast<const float4*>(Ws + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
+                w[i][2 * j] = make_float2(v.x, v.y);
+                w[i][2 * j + 1] = make_float2(v.z, v.w);
+            }
+        }
+    }
+
+    if (tid == 0) {
+        mbar_init(&sm.xbar[0], 1);
+        mbar_init(&sm.xbar[1], 1);
+        fence_mbar_init();
+        if (T > 0) {
+            prefetch_tensormap(&tmx);
+            prefetch_tensormap(&tmy);
+        }
+    }
+    __syncthreads();
+
+    // ---- x staging (warp XW) and its TMA bookkeeping
+    int issued = -1, landed = -1;
+    constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
+    auto issue_chunk = [&](int c) {
+        if (lane == 0 && c != kp.skip_chunk) {
+            mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
+            tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, c * TAU, b);
+        }
+        issued = c;
+    };
+    auto stage_x = [&](int tn, float* dst) {
+        float v0 = 0.f, v1 = 0.f;
+        if (tn < T) {
+            const float* src = sm.xring[(tn / TAU) & 1][tn % TAU];
+            v0 = src[lane];
+            v1 = src[lane + 32];
+            if constexpr (SMX) softmax64(v0, v1, v0, v1);
+        }
+        dst[lane] = v0;
+        dst[lane + 32] = v1;
+    };
+
+    int fail = 0;
+    if (warp == XW && T > 0) {
+        issue_chunk(0);
+        if (nchunks > 1) issue_chunk(1);
+        if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], 0, kp.wait_limit_ns))) {
+            landed = 0;
+            stage_x(0, sm.xs[0]);
+            stage_x(1, sm.xs[1]);
+        } else {
+            fail = 1;
+        }
+    }
+    int abort = __syncthreads_or(fail);
+
+    // ---- prologue: z_0 = W_0 x~_0
+    if (!abort && T > 0) {
+        float2 x2[NP];
+        load_pairs(sm.xs[0], cg, x2);
+        float2 acc[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if (i == SLOTS && !has_beta) continue;
+                acc[i] = __ffma2_rn(w[i][q], x2[q], acc[i]);
+            }
+        }
+        float bb[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) bb[i] = acc[i].x + acc[i].y;
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < S1; ++i) bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
+        }
+#pragma unroll
+        for (int i = 0; i < S1; ++i) {
+            if ((i & 3) != cg) continue;
+            if (i < 2) sm.ystage[0][0][rg + 32 * i] = bb[i];
+            else if (i < SLOTS) sm.z[0][rg + 32 * i] = bb[i];
+            else if (has_beta && 3 * D + rg < M) sm.z[0][3 * D + rg] = bb[i];
+        }
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+
+    // the pending rank-one update (applied at the start of the next step)
+    float coef[S1];
+#pragma unroll
+    for (int i = 0; i < S1; ++i) coef[i] = 0.f;
+    float2 pkc[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) pkc[q] = make_float2(0.f, 0.f);
+
+    for (int t = 0; t < T && !abort; ++t) {
+        // y chunk holding y_t complete -> TMA store
+        if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
+            const int c = t / TAU;
+            tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, c * TAU, b);
+            bulk_commit();
+            bulk_wait_read<1>();
+        }
+
+        // ---- 1. softmax / gates (every warp) || pending update + b-dots
+        const float* zt = sm.z[t & 1];
+        float* zn = sm.z[(t + 1) & 1];
+        const float k0 = zt[D + lane], k1 = zt[D + 32 + lane];
+        const float q0 = zt[2 * D + lane], q1 = zt[2 * D + 32 + lane];
+        const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
+
+        float2 x2[NP];
+        load_pairs(sm.xs[(t + 1) & 1], cg, x2);
+        float2 accb[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) accb[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if (i == SLOTS && !has_beta) continue;
+                w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
+            }
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if (i == SLOTS && !has_beta) continue;
+                accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
+            }
+        }
+
+        float pk0, pk1, pq0, pq1;
+        softmax64(k0, k1, pk0, pk1);
+        softmax64(q0, q1, pq0, pq1);
+        float g[4];
+        if constexpr (NLR == 4) {
+            g[0] = sigmoid_fast(beta.x);
+            g[1] = sigmoid_fast(beta.y);
+            g[2] = sigmoid_fast(beta.z);
+            g[3] = sigmoid_fast(beta.w);
+        } else {
+            g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
+        }
+
+        // ---- 2. phi into the thread's column layout; a-dots; partial phi_k . x~
+        float* pkq = &sm.pkq[warp][0][0];
+        pkq[lane] = pk0;
+        pkq[lane + 32] = pk1;
+        pkq[D + lane] = pq0;
+        pkq[D + lane + 32] = pq1;
+        __syncwarp();
+        float2 u2[NP];
+        {
+            float2 q2[NP];
+            load_pairs(pkq, cg, pkc);
+            load_pairs(pkq + D, cg, q2);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) u2[q] = make_float2(q2[q].x - pkc[q].x, q2[q].y - pkc[q].y);
+        }
+        float2 acca[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) acca[i] = make_float2(0.f, 0.f);
+        float2 accs = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if (i == SLOTS && !has_beta) continue;
+                acca[i] = __ffma2_rn(w[i][q], u2[q], acca[i]);
+            }
+            accs = __ffma2_rn(pkc[q], x2[q], accs);
+        }
+        float a[S1], bb[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) {
+            a[i] = acca[i].x + acca[i].y;
+            bb[i] = accb[i].x + accb[i].y;
+        }
+        float s = accs.x + accs.y;
+
+        // ---- 3. finish the dots over the 4 column groups
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if (i == SLOTS && !has_beta) continue;
+                a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
+                bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
+            }
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        }
+
+        const bool write_y = (t + 1 < T);
+        float* yrow = sm.ystage[((t + 1) / TAU) % 3][(t + 1) % TAU];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) {
+            if (i == SLOTS && !has_beta) {
+                coef[i] = 0.f;
+                continue;
+            }
+            const int blk = (NLR == 1) ? 0 : (i < SLOTS ? i / 2 : 3);
+            coef[i] = g[blk] * a[i];
+            const float zr = fmaf(coef[i], s, bb[i]);
+            if ((i & 3) == cg) {
+                if (i < 2) {
+                    if (write_y) yrow[rg + 32 * i] = zr;
+                } else if (i < SLOTS) {
+                    zn[rg + 32 * i] = zr;
+                } else if (3 * D + rg < M) {
+                    zn[3 * D + rg] = zr;
+                }
+            }
+        }
+        if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+
+        // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
+        fail = 0;
+        if (warp == XW) {
+            const int tn = t + 2;
+            if (tn < T && tn % TAU == 0) {
+                const int c = tn / TAU;
+                const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
+                if (__all_sync(0xffffffffu, ok)) {
+                    landed = c;
+                    if (c + 1 < nchunks) issue_chunk(c + 1);
+                } else {
+                    fail = 1;
+                }
+            }
+            if (!fail) stage_x(tn, sm.xs[t & 1]);
+        }
+        abort = __syncthreads_or(fail);
+    }
+
+    // ---- drain
+    if (warp == 0 && lane == 0) {
+        if (!abort && T > 0 && T % TAU != 0) {
+            const int c = (T - 1) / TAU;
+            tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, c * TAU, b);
+            bulk_commit();
+        }
+        bulk_wait_all<0>();
+    }
+    if (warp == XW && abort) {
+        // every load still in flight lands before the CTA gives up its shared memory
+        for (int c = landed + 1; c <= issued; ++c) {
+            if (c == kp.skip_chunk) continue;
+            mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
+        }
+        if (lane == 0) atomicOr(kp.status, kStatusTimeout);
+    }
+    if (abort) return;
+
+    // ---- the last pending update, then W_T -> W_out[b, h]
+    float* Wd = kp.W_out + static_cast<size_t>(p) * M * D;
+#pragma unroll
+    for (int i = 0; i < S1; ++i) {
+        const int r = (i < SLOTS) ? rg + 32 * i : 3 * D + rg;
+        if (i == SLOTS && !(has_beta && r < M)) continue;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j) {
+            *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
+                make_float4(w[i][2 * j].x, w[i][2 * j].y, w[i][2 * j + 1].x, w[i][2 * j + 1].y);
+        }
+    }
+}
+
+template <int NLR, bool SMX>
+LaunchInfo launch_info_d64_impl()
+{
+    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64_kernel<NLR, SMX>), d64::NT, 1,
+                      static_cast<int>(sizeof(d64::Smem)) + 128, d64::TAU};
+}
+
+}  // namespace srwm
