@@ -118,6 +118,117 @@ __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&o
 
 }  // namespace d64
 
+// One step of the recurrence for a warp whose threads carry NS row slots
+// (slots 0..5: rows rg + 32 i; slot 6: beta row 192 + rg).  Reads z_t, phi
+// inputs and x~_{t+1} from shared memory, applies the pending update, writes
+// z_{t+1} (y rows to the staging buffer) and leaves this step's update pending
+// in (coef, pkc).
+template <int NS, int NLR>
+__device__ __forceinline__ void d64_step(d64::Smem& sm, int t, int T, int lane, int warp, int rg, int cg,
+                                         float2 (&w)[d64::SLOTS + 1][d64::NP], float (&coef)[d64::SLOTS + 1],
+                                         float2 (&pkc)[d64::NP])
+{
+    using namespace d64;
+    constexpr int M = 3 * D + NLR;
+    const float* zt = sm.z[t & 1];
+    float* zn = sm.z[(t + 1) & 1];
+
+    // ---- 1. softmax / gates || pending update + b-dots
+    const float k0 = zt[D + lane], k1 = zt[D + 32 + lane];
+    const float q0 = zt[2 * D + lane], q1 = zt[2 * D + 32 + lane];
+    const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
+
+    float2 x2[NP];
+    load_pairs(sm.xs[(t + 1) & 1], cg, x2);
+    float2 accb[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) accb[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+            w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
+            accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
+        }
+    }
+
+    float pk0, pk1, pq0, pq1;
+    softmax64(k0, k1, pk0, pk1);
+    softmax64(q0, q1, pq0, pq1);
+    float g[4];
+    if constexpr (NLR == 4) {
+        g[0] = sigmoid_fast(beta.x);
+        g[1] = sigmoid_fast(beta.y);
+        g[2] = sigmoid_fast(beta.z);
+        g[3] = sigmoid_fast(beta.w);
+    } else {
+        g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
+    }
+
+    // ---- 2. phi into the thread's column layout; a-dots; partial phi_k . x~
+    float* pkq = &sm.pkq[warp][0][0];
+    pkq[lane] = pk0;
+    pkq[lane + 32] = pk1;
+    pkq[D + lane] = pq0;
+    pkq[D + lane + 32] = pq1;
+    __syncwarp();
+    float2 u2[NP];
+    {
+        float2 q2[NP];
+        load_pairs(pkq, cg, pkc);
+        load_pairs(pkq + D, cg, q2);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) u2[q] = make_float2(q2[q].x - pkc[q].x, q2[q].y - pkc[q].y);
+    }
+    float2 acca[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acca[i] = make_float2(0.f, 0.f);
+    float2 accs = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) acca[i] = __ffma2_rn(w[i][q], u2[q], acca[i]);
+        accs = __ffma2_rn(pkc[q], x2[q], accs);
+    }
+    float a[NS], bb[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        a[i] = acca[i].x + acca[i].y;
+        bb[i] = accb[i].x + accb[i].y;
+    }
+    float s = accs.x + accs.y;
+
+    // ---- 3. finish the dots over the 4 column groups; store z_{t+1}
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+            a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
+            bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+    }
+
+    const bool write_y = (t + 1 < T);
+    float* yrow = sm.ystage[((t + 1) / TAU) % 3][(t + 1) % TAU];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int blk = (NLR == 1) ? 0 : (i < SLOTS ? i / 2 : 3);
+        coef[i] = g[blk] * a[i];
+        const float zr = fmaf(coef[i], s, bb[i]);
+        if ((i & 3) == cg) {
+            if (i < 2) {
+                if (write_y) yrow[rg + 32 * i] = zr;
+            } else if (i < SLOTS) {
+                zn[rg + 32 * i] = zr;
+            } else if (3 * D + rg < M) {
+                zn[3 * D + rg] = zr;
+            }
+        }
+    }
+    if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+}
+
 template <int NLR, bool SMX>
 __global__ void __launch_bounds__(d64::NT, 2)
     srwm_d64_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
@@ -252,116 +363,10 @@ __global__ void __launch_bounds__(d64::NT, 2)
             bulk_commit();
             bulk_wait_read<1>();
         }
-
-        // ---- 1. softmax / gates (every warp) || pending update + b-dots
-        const float* zt = sm.z[t & 1];
-        float* zn = sm.z[(t + 1) & 1];
-        const float k0 = zt[D + lane], k1 = zt[D + 32 + lane];
-        const float q0 = zt[2 * D + lane], q1 = zt[2 * D + 32 + lane];
-        const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
-
-        float2 x2[NP];
-        load_pairs(sm.xs[(t + 1) & 1], cg, x2);
-        float2 accb[S1];
-#pragma unroll
-        for (int i = 0; i < S1; ++i) accb[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-#pragma unroll
-            for (int i = 0; i < S1; ++i) {
-                if (i == SLOTS && !has_beta) continue;
-                w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
-            }
-#pragma unroll
-            for (int i = 0; i < S1; ++i) {
-                if (i == SLOTS && !has_beta) continue;
-                accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
-            }
-        }
-
-        float pk0, pk1, pq0, pq1;
-        softmax64(k0, k1, pk0, pk1);
-        softmax64(q0, q1, pq0, pq1);
-        float g[4];
-        if constexpr (NLR == 4) {
-            g[0] = sigmoid_fast(beta.x);
-            g[1] = sigmoid_fast(beta.y);
-            g[2] = sigmoid_fast(beta.z);
-            g[3] = sigmoid_fast(beta.w);
-        } else {
-            g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
-        }
-
-        // ---- 2. phi into the thread's column layout; a-dots; partial phi_k . x~
-        float* pkq = &sm.pkq[warp][0][0];
-        pkq[lane] = pk0;
-        pkq[lane + 32] = pk1;
-        pkq[D + lane] = pq0;
-        pkq[D + lane + 32] = pq1;
-        __syncwarp();
-        float2 u2[NP];
-        {
-            float2 q2[NP];
-            load_pairs(pkq, cg, pkc);
-            load_pairs(pkq + D, cg, q2);
-#pragma unroll
-            for (int q = 0; q < NP; ++q) u2[q] = make_float2(q2[q].x - pkc[q].x, q2[q].y - pkc[q].y);
-        }
-        float2 acca[S1];
-#pragma unroll
-        for (int i = 0; i < S1; ++i) acca[i] = make_float2(0.f, 0.f);
-        float2 accs = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-#pragma unroll
-            for (int i = 0; i < S1; ++i) {
-                if (i == SLOTS && !has_beta) continue;
-                acca[i] = __ffma2_rn(w[i][q], u2[q], acca[i]);
-            }
-            accs = __ffma2_rn(pkc[q], x2[q], accs);
-        }
-        float a[S1], bb[S1];
-#pragma unroll
-        for (int i = 0; i < S1; ++i) {
-            a[i] = acca[i].x + acca[i].y;
-            bb[i] = accb[i].x + accb[i].y;
-        }
-        float s = accs.x + accs.y;
-
-        // ---- 3. finish the dots over the 4 column groups
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-#pragma unroll
-            for (int i = 0; i < S1; ++i) {
-                if (i == SLOTS && !has_beta) continue;
-                a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
-                bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
-            }
-            s += __shfl_xor_sync(0xffffffffu, s, o);
-        }
-
-        const bool write_y = (t + 1 < T);
-        float* yrow = sm.ystage[((t + 1) / TAU) % 3][(t + 1) % TAU];
-#pragma unroll
-        for (int i = 0; i < S1; ++i) {
-            if (i == SLOTS && !has_beta) {
-                coef[i] = 0.f;
-                continue;
-            }
-            const int blk = (NLR == 1) ? 0 : (i < SLOTS ? i / 2 : 3);
-            coef[i] = g[blk] * a[i];
-            const float zr = fmaf(coef[i], s, bb[i]);
-            if ((i & 3) == cg) {
-                if (i < 2) {
-                    if (write_y) yrow[rg + 32 * i] = zr;
-                } else if (i < SLOTS) {
-                    zn[rg + 32 * i] = zr;
-                } else if (3 * D + rg < M) {
-                    zn[3 * D + rg] = zr;
-                }
-            }
-        }
-        if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+        // Warp 0 also carries the beta rows (slot 6); a compile-time slot count
+        // keeps each role's step free of branches.
+        if (has_beta) d64_step<S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
+        else d64_step<SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
 
         // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
         fail = 0;
