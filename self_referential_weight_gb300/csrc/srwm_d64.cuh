@@ -11,10 +11,12 @@
 // so y_{t+1} = z_{t+1}[0:64] is still read from the pre-update matrix of its
 // own step (W_t).
 //
-// Layout.  Thread (rg = tid/4, cg = tid%4) holds rows rg + 32 i (i = 0..5:
-// blocks y, y, k, k, q, q) and, in warp 0, row 192 + rg (beta rows, valid for
-// rg < n_lr), over the 16 columns of float4 chunks cg, cg+4, cg+8, cg+12, kept
-// as float2 pairs for the two-wide FMA.  W never leaves registers.
+// Layout.  A stream has NW warps (4, or 8 when there are fewer streams than
+// SMs and a stream should use a whole SM), i.e. RG = 8 NW row groups.  Thread
+// (rg = tid/4, cg = tid%4) holds rows rg + RG i (i < 192/RG: blocks y, k, q in
+// order) and, in warp 0, row 192 + rg (beta rows, valid for rg < n_lr), over
+// the 16 columns of float4 chunks cg, cg+4, cg+8, cg+12, kept as float2 pairs
+// for the two-wide FMA.  W never leaves registers.
 //
 // One step, one CTA barrier:
 //   1. every warp computes phi_k, phi_q and the gates from z_t in shared
@@ -46,18 +48,30 @@ namespace srwm {
 namespace d64 {
 
 constexpr int D = 64;
-constexpr int NT = 128;     // threads per CTA (one stream)
-constexpr int SLOTS = 6;    // row slots of every thread (rows 0..191)
 constexpr int TAU = 32;     // steps per TMA chunk
 constexpr int NP = 8;       // float2 column pairs per thread
-constexpr int XW = 3;       // warp staging x~ and driving the x TMA ring
 
+// NW warps per stream: RG row groups, SLOTS row slots of every thread (rows
+// 0..191), one more slot in warp 0 for the beta rows.
+template <int NW_>
+struct Cfg {
+    static constexpr int NW = NW_;
+    static constexpr int NT = 32 * NW;
+    static constexpr int RG = 8 * NW;
+    static constexpr int SLOTS = 3 * D / RG;
+    static constexpr int XW = NW - 1;   // warp staging x~ and driving the x TMA ring
+    static_assert(NW == 4 || NW == 8, "4 or 8 warps per stream");
+    // row block (0 y, 1 k, 2 q) of slot i
+    SRWM_HD static constexpr int block_of_slot(int i) { return (RG * i) / D; }
+};
+
+template <int NW>
 struct __align__(128) Smem {
     float xring[2][TAU][D];    // TMA destination: raw x, two chunks
     float ystage[3][TAU][D];   // TMA source: y, three chunks
     float z[2][D * 3 + 8];     // k, q, beta rows of z_t by step parity (index = row)
     float xs[2][D];            // x~_{t+1}, x~_{t+2}
-    float pkq[4][2][D];        // per warp: phi_k, phi_q in plain column order
+    float pkq[NW][2][D];       // per warp: phi_k, phi_q in plain column order
     uint64_t xbar[2];          // "chunk landed" barriers of the x ring
 };
 
@@ -119,16 +133,18 @@ __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&o
 }  // namespace d64
 
 // One step of the recurrence for a warp whose threads carry NS row slots
-// (slots 0..5: rows rg + 32 i; slot 6: beta row 192 + rg).  Reads z_t, phi
+// (slots i < SLOTS: rows rg + RG i; slot SLOTS: beta row 192 + rg).  Reads z_t, phi
 // inputs and x~_{t+1} from shared memory, applies the pending update, writes
 // z_{t+1} (y rows to the staging buffer) and leaves this step's update pending
 // in (coef, pkc).
-template <int NS, int NLR>
-__device__ __forceinline__ void d64_step(d64::Smem& sm, int t, int T, int lane, int warp, int rg, int cg,
-                                         float2 (&w)[d64::SLOTS + 1][d64::NP], float (&coef)[d64::SLOTS + 1],
-                                         float2 (&pkc)[d64::NP])
+template <int NW, int NS, int NLR>
+__device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int lane, int warp, int rg, int cg,
+                                         float2 (&w)[d64::Cfg<NW>::SLOTS + 1][d64::NP],
+                                         float (&coef)[d64::Cfg<NW>::SLOTS + 1], float2 (&pkc)[d64::NP])
 {
     using namespace d64;
+    using C = Cfg<NW>;
+    constexpr int SLOTS = C::SLOTS, RG = C::RG;
     constexpr int M = 3 * D + NLR;
     const float* zt = sm.z[t & 1];
     float* zn = sm.z[(t + 1) & 1];
@@ -213,14 +229,14 @@ __device__ __forceinline__ void d64_step(d64::Smem& sm, int t, int T, int lane, 
     float* yrow = sm.ystage[((t + 1) / TAU) % 3][(t + 1) % TAU];
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-        const int blk = (NLR == 1) ? 0 : (i < SLOTS ? i / 2 : 3);
+        const int blk = (NLR == 1) ? 0 : (i < SLOTS ? C::block_of_slot(i) : 3);
         coef[i] = g[blk] * a[i];
         const float zr = fmaf(coef[i], s, bb[i]);
         if ((i & 3) == cg) {
-            if (i < 2) {
-                if (write_y) yrow[rg + 32 * i] = zr;
+            if (i < SLOTS && C::block_of_slot(i) == 0) {
+                if (write_y) yrow[rg + RG * i] = zr;
             } else if (i < SLOTS) {
-                zn[rg + 32 * i] = zr;
+                zn[rg + RG * i] = zr;
             } else if (3 * D + rg < M) {
                 zn[3 * D + rg] = zr;
             }
@@ -229,16 +245,18 @@ __device__ __forceinline__ void d64_step(d64::Smem& sm, int t, int T, int lane, 
     if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
 }
 
-template <int NLR, bool SMX>
-__global__ void __launch_bounds__(d64::NT, 2)
+template <int NW, int NLR, bool SMX>
+__global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     srwm_d64_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                     const KParams kp)
 {
     using namespace d64;
+    using C = Cfg<NW>;
+    constexpr int SLOTS = C::SLOTS, RG = C::RG, XW = C::XW;
     constexpr int M = 3 * D + NLR;
     constexpr int S1 = SLOTS + 1;
     extern __shared__ unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    Smem<NW>& sm = *reinterpret_cast<Smem<NW>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 2, cg = tid & 3;
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(d64::NT, 2)
         const float* Ws = kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * M * D;
 #pragma unroll
         for (int i = 0; i < S1; ++i) {
-            const int r = (i < SLOTS) ? rg + 32 * i : 3 * D + rg;
+            const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
             const bool ok = (i < SLOTS) || (has_beta && r < M);
 #pragma unroll
             for (int j = 0; j < NP / 2; ++j) {
@@ -339,8 +357,8 @@ __global__ void __launch_bounds__(d64::NT, 2)
 #pragma unroll
         for (int i = 0; i < S1; ++i) {
             if ((i & 3) != cg) continue;
-            if (i < 2) sm.ystage[0][0][rg + 32 * i] = bb[i];
-            else if (i < SLOTS) sm.z[0][rg + 32 * i] = bb[i];
+            if (i < SLOTS && C::block_of_slot(i) == 0) sm.ystage[0][0][rg + RG * i] = bb[i];
+            else if (i < SLOTS) sm.z[0][rg + RG * i] = bb[i];
             else if (has_beta && 3 * D + rg < M) sm.z[0][3 * D + rg] = bb[i];
         }
         fence_proxy_async_smem();
@@ -365,8 +383,8 @@ __global__ void __launch_bounds__(d64::NT, 2)
         }
         // Warp 0 also carries the beta rows (slot 6); a compile-time slot count
         // keeps each role's step free of branches.
-        if (has_beta) d64_step<S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
-        else d64_step<SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
+        if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
+        else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
 
         // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
         fail = 0;
@@ -410,7 +428,7 @@ __global__ void __launch_bounds__(d64::NT, 2)
     float* Wd = kp.W_out + static_cast<size_t>(p) * M * D;
 #pragma unroll
     for (int i = 0; i < S1; ++i) {
-        const int r = (i < SLOTS) ? rg + 32 * i : 3 * D + rg;
+        const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
         if (i == SLOTS && !(has_beta && r < M)) continue;
 #pragma unroll
         for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
@@ -422,11 +440,11 @@ __global__ void __launch_bounds__(d64::NT, 2)
     }
 }
 
-template <int NLR, bool SMX>
+template <int NW, int NLR, bool SMX>
 LaunchInfo launch_info_d64_impl()
 {
-    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64_kernel<NLR, SMX>), d64::NT, 1,
-                      static_cast<int>(sizeof(d64::Smem)) + 128, d64::TAU};
+    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64_kernel<NW, NLR, SMX>), d64::Cfg<NW>::NT, 1,
+                      static_cast<int>(sizeof(d64::Smem<NW>)) + 128, d64::TAU};
 }
 
 }  // namespace srwm

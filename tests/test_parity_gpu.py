@@ -203,3 +203,16 @@ def test_binding_raises_on_error():
     with pytest.raises(binding.SrwmError) as e:
         binding.srwm_forward(x, W0, 4)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
+def test_d64_more_streams_than_sms(n_lr, smx):
+    """d = 64 with more (b, h) streams than SMs (the four-warp-per-stream
+    variant; fewer streams use eight warps each), checked in full."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    B = n_sm // 8 + 3
+    wl = inputs.Workload("t", B, 40, 8, 64, n_lr, smx, 77, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
