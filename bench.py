@@ -37,7 +37,7 @@ UNIT = "head-token updates/s"
 FMA_PER_CLK_PER_SM = 128          # FP32 FMA lanes per SM (4 SMSPs x 32)
 L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "srwm_cta_kernel_mid.md")
-KERNEL_SOURCES = ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"]
+KERNEL_SOURCES = ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"]
 
 
 def parse():

@@ -70,6 +70,25 @@ int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, in
                  int softmax_input, float* y_out, float* W_final, void* stream);
 
 /*
+ * srwm_forward_from -- srwm_forward from a per-sequence state instead of the
+ * shared W0: the state carried across truncation windows, e.g. RL rollouts
+ * that keep W_t until the episode ends (review of "A Modern Self-Referential
+ * Weight Matrix That Learns to Modify Itself", section 4.5, on keeping the
+ * self-modified state across 50-step windows).  Running T1 steps with
+ * srwm_forward and the remaining T - T1 steps with srwm_forward_from on the
+ * returned W_final reproduces one srwm_forward over all T steps.
+ *
+ *   x        [B, T, H, d]   this window's inputs
+ *   W_init   [B, H, m, d]   state of every stream at the start of the window (read)
+ *   y_out    [B, T, H, d]   written
+ *   W_final  [B, H, m, d]   written; may be the same pointer as W_init (in
+ *                           place) but must not partially overlap it
+ * Other arguments, rules and return values as srwm_forward.
+ */
+int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, int d, int n_lr,
+                      int softmax_input, float* y_out, float* W_final, void* stream);
+
+/*
  * srwm_step -- one step of the same recurrence from a per-sequence state:
  * W_out[b,h] = W_in[b,h] + update, y_t[b,h] = y from W_in[b,h].  Calling it T
  * times, feeding W_out back as W_in, reproduces srwm_forward.

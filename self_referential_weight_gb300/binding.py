@@ -18,7 +18,7 @@ _LIB = None
 SRWM_OK = 0
 SRWM_ERR_TIMEOUT = 7
 
-EXPORTS = ("srwm_forward", "srwm_step", "srwm_status_string", "srwm_last_device_status",
+EXPORTS = ("srwm_forward", "srwm_forward_from", "srwm_step", "srwm_status_string", "srwm_last_device_status",
            "srwm_set_wait_limit_ns", "srwm_debug_skip_x_chunk", "srwm_probe_fma")
 
 
@@ -45,6 +45,8 @@ def _lib():
         P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
         lib.srwm_forward.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward.restype = I
+        lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
+        lib.srwm_forward_from.restype = I
         lib.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
         lib.srwm_step.restype = I
         lib.srwm_status_string.argtypes = [I]
@@ -107,6 +109,23 @@ def srwm_forward(x, W0, n_lr, softmax_input=False, y_out=None, W_final=None, str
     rc = _lib().srwm_forward(px, pw, B, T, H, d, int(n_lr), int(bool(softmax_input)), py, pf,
                              _stream_handle(stream))
     _check(rc, "srwm_forward")
+    return y_out, W_final
+
+
+def srwm_forward_from(x, W_init, n_lr, softmax_input=False, y_out=None, W_final=None, stream=None):
+    """T steps starting from per-sequence states W_init [B,H,m,d] (state carry).
+
+    Returns (y [B,T,H,d], W_final [B,H,m,d]); W_final may be W_init itself."""
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    if y_out is None:
+        y_out = torch.empty((B, T, H, d), dtype=torch.float32, device=x.device)
+    if W_final is None:
+        W_final = torch.empty((B, H, m, d), dtype=torch.float32, device=W_init.device)
+    rc = _lib().srwm_forward_from(_dev(x, "x"), _dev(W_init, "W_init", (B, H, m, d)), B, T, H, d,
+                                  int(n_lr), int(bool(softmax_input)), _dev(y_out, "y_out", (B, T, H, d)),
+                                  _dev(W_final, "W_final", (B, H, m, d)), _stream_handle(stream))
+    _check(rc, "srwm_forward_from")
     return y_out, W_final
 
 

@@ -215,6 +215,16 @@ int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, in
                static_cast<cudaStream_t>(stream));
 }
 
+int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, int d, int n_lr,
+                      int softmax_input, float* y_out, float* W_final, void* stream)
+{
+    if (!W_init || !W_final || (T > 0 && (!x || !y_out))) return SRWM_ERR_NULL;
+    const int rc = check_params(B, T, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    return run(x, W_init, 1, B, T, H, d, n_lr, softmax_input, y_out, W_final,
+               static_cast<cudaStream_t>(stream));
+}
+
 int srwm_step(const float* x_t, const float* W_in, int B, int H, int d, int n_lr,
               int softmax_input, float* y_t, float* W_out, void* stream)
 {

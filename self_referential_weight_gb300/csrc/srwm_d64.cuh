@@ -75,51 +75,6 @@ struct __align__(128) Smem {
     uint64_t xbar[2];          // "chunk landed" barriers of the x ring
 };
 
-__device__ __forceinline__ float redux_max(float v)
-{
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t redux_add(uint32_t v)
-{
-    uint32_t r;
-    asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-    return r;
-}
-
-__device__ __forceinline__ float rcp_approx(float v)
-{
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
-    return r;
-}
-
-// Warp sum of two values in [0, 1] per lane, exact in fixed point with 2^-31
-// resolution (16-bit halves keep the u32 sums from overflowing).  Every lane
-// gets the same bits whatever the order of lanes.
-__device__ __forceinline__ float warp_sum_unit(float e0, float e1)
-{
-    const uint32_t q0 = __float2uint_rn(e0 * 2147483648.0f);
-    const uint32_t q1 = __float2uint_rn(e1 * 2147483648.0f);
-    const uint32_t hi = redux_add((q0 >> 16) + (q1 >> 16));
-    const uint32_t lo = redux_add((q0 & 0xffffu) + (q1 & 0xffffu));
-    return fmaf(static_cast<float>(hi), 3.0517578125e-05f, static_cast<float>(lo) * 4.656612873077393e-10f);
-}
-
-// softmax over 64 values held as (v0, v1) = entries (lane, lane + 32).
-__device__ __forceinline__ void softmax64(float v0, float v1, float& p0, float& p1)
-{
-    const float mx = redux_max(fmaxf(v0, v1));
-    const float e0 = __expf(v0 - mx), e1 = __expf(v1 - mx);
-    const float inv = rcp_approx(warp_sum_unit(e0, e1));
-    p0 = e0 * inv;
-    p1 = e1 * inv;
-}
-
-__device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.0f + __expf(-v)); }
-
 __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&out)[NP])
 {
 #pragma unroll

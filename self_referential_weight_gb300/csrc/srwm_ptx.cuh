@@ -138,4 +138,61 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
+// ---------------------------------------------------------------- fast softmax pieces
+// (shared by the kernels; results are identical on every lane of the warp)
+__device__ __forceinline__ float redux_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t redux_add(uint32_t v)
+{
+    uint32_t r;
+    asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float v)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Warp sum of one value in [0, 1] per lane, exact in fixed point (2^-31 steps).
+__device__ __forceinline__ float warp_sum_unit1(float e)
+{
+    const uint32_t q = __float2uint_rn(e * 2147483648.0f);
+    const uint32_t hi = redux_add(q >> 16);
+    const uint32_t lo = redux_add(q & 0xffffu);
+    return fmaf(static_cast<float>(hi), 3.0517578125e-05f, static_cast<float>(lo) * 4.656612873077393e-10f);
+}
+
+// Warp sum of two values in [0, 1] per lane, exact in fixed point with 2^-31
+// resolution (16-bit halves keep the u32 sums from overflowing).  Every lane
+// gets the same bits whatever the order of lanes.
+__device__ __forceinline__ float warp_sum_unit(float e0, float e1)
+{
+    const uint32_t q0 = __float2uint_rn(e0 * 2147483648.0f);
+    const uint32_t q1 = __float2uint_rn(e1 * 2147483648.0f);
+    const uint32_t hi = redux_add((q0 >> 16) + (q1 >> 16));
+    const uint32_t lo = redux_add((q0 & 0xffffu) + (q1 & 0xffffu));
+    return fmaf(static_cast<float>(hi), 3.0517578125e-05f, static_cast<float>(lo) * 4.656612873077393e-10f);
+}
+
+// softmax over 64 values held as (v0, v1) = entries (lane, lane + 32).
+__device__ __forceinline__ void softmax64(float v0, float v1, float& p0, float& p1)
+{
+    const float mx = redux_max(fmaxf(v0, v1));
+    const float e0 = __expf(v0 - mx), e1 = __expf(v1 - mx);
+    const float inv = rcp_approx(warp_sum_unit(e0, e1));
+    p0 = e0 * inv;
+    p1 = e1 * inv;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.0f + __expf(-v)); }
+
+
 }  // namespace srwm

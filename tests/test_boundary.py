@@ -106,3 +106,18 @@ def test_oracle_library_is_separate():
     for n in names:
         assert not hasattr(lib, n)
     assert oracle.lib_path() != lib_build.LIB
+
+
+def test_forward_from_validation(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
+    ok = dict(x=A, W=A + 0x1000000, y=A + 0x2000000, Wf=A + 0x3000000)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.srwm_forward_from(a["x"], a["W"], 2, 3, 2, 16, 4, 0, a["y"], a["Wf"], None)
+
+    assert call(W=None) == 1
+    assert call(x=A + 4) == 4
+    assert call(Wf=A + 0x1000000 + 16) == 5      # partial overlap of W_final with W_init
+    assert lib.srwm_forward_from(A, A + 0x1000000, 2, 3, 2, 48, 4, 0, A + 0x2000000, A + 0x3000000, None) == 3

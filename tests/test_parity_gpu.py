@@ -216,3 +216,34 @@ def test_d64_more_streams_than_sms(n_lr, smx):
     y, Wf = run_gpu(x, W0, n_lr, smx)
     yo, Wo = oracle.forward(x, W0, n_lr, smx)
     assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
+def test_forward_from_resumes_a_split_sequence(d, n_lr, smx):
+    """State carry: T1 steps of srwm_forward, then T - T1 steps of
+    srwm_forward_from on the returned state (in place), equal one call over T
+    steps; the second window also matches the oracle started from its state."""
+    wl = inputs.Workload("t", 3, 70, 2, d, n_lr, smx, 90 + d, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    T1 = 37
+    y_full, Wf_full = run_gpu(x, W0, n_lr, smx)
+    xd = torch.from_numpy(x).to(DEV)
+    y1, W = binding.srwm_forward(xd[:, :T1].contiguous(), torch.from_numpy(W0).to(DEV), n_lr, smx)
+    W_mid = W.cpu().numpy()
+    y2, W = binding.srwm_forward_from(xd[:, T1:].contiguous(), W, n_lr, smx, W_final=W)
+    torch.cuda.synchronize()
+    assert binding.srwm_last_device_status() == 0
+    y_split = np.concatenate([y1.cpu().numpy(), y2.cpu().numpy()], axis=1)
+    assert rel(y_split, y_full) <= 1e-5
+    assert rel(W.cpu().numpy(), Wf_full) <= 1e-5
+    yo, Wo = oracle.forward(np.ascontiguousarray(x[:, T1:]), W_mid, n_lr, smx, per_sequence=True)
+    assert rel(y2.cpu().numpy(), yo) <= 1e-4 and rel(W.cpu().numpy(), Wo) <= 1e-4
+
+
+def test_forward_from_zero_steps_copies_state():
+    W = torch.randn(2, 3, 52, 16, device=DEV)
+    x = torch.empty((2, 0, 3, 16), device=DEV)
+    _, Wf = binding.srwm_forward_from(x, W, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(Wf, W)
