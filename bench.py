@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of the SRWM forward recurrence on GB300.
 
-One step = one srwm_forward call over the whole workload (every row of the hot
+One step = one srwm_forward_balanced call over the whole workload (every row of the hot
 path: input softmax when enabled, Eq. (1) read-out, phi of k and q, gates,
 fused Eq. (2)/(3) update).  Default workload: "mid" (B=64, T=1024, H=8, d=64,
 four learning rates), the d = 64 configuration the FP32-FMA target is stated
@@ -251,8 +251,11 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    workspace = torch.empty(binding.srwm_forward_workspace_bytes(wl.B, wl.H), dtype=torch.uint8, device=dev)
+
     def step():
-        binding.srwm_forward(x, W0, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, stream=stream)
+        binding.srwm_forward_balanced(x, W0, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf,
+                                      workspace=workspace, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -303,7 +306,8 @@ def main():
     def e2e_step():
         xd.copy_(x_h, non_blocking=True)
         W0d.copy_(W0_h, non_blocking=True)
-        binding.srwm_forward(xd, W0d, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, stream=stream)
+        binding.srwm_forward_balanced(xd, W0d, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf,
+                                      workspace=workspace, stream=stream)
         y_h.copy_(y, non_blocking=True)
         Wf_h.copy_(Wf, non_blocking=True)
 
@@ -374,7 +378,7 @@ def main():
             "unit": "TFLOP/s",
             "frac": achieved / peak_tflops,
             "traffic": profiled_traffic(wl.name),
-            "kernel": "srwm_cta_kernel" if wl.d == 64 else "srwm_warp_kernel",
+            "kernel": "srwm_d64_kernel" if wl.d == 64 else "srwm_warp_kernel",
             "flops_per_launch": flops_per_launch,
             "peak_basis": f"{n_sm} SMs x {FMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 flop x "
                           f"{f_max_mhz:.0f} MHz (max SM clock)",

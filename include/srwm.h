@@ -34,6 +34,8 @@
 #ifndef SRWM_H
 #define SRWM_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -68,6 +70,31 @@ enum srwm_status {
  */
 int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
                  int softmax_input, float* y_out, float* W_final, void* stream);
+
+/*
+ * srwm_forward_balanced -- srwm_forward (same arguments, same results within
+ * fp32 rounding) on a load-balanced schedule, for workloads with more
+ * (sequence, head) streams than the GPU holds at once.  Every stream's T steps
+ * are cut into segments (a multiple of 32 steps); a persistent cooperative
+ * grid processes (stream, segment) items in segment-major order, handing each
+ * stream's state from one segment to the next through W_final.  This replaces
+ * a mostly empty last wave of whole streams by rounds of short segments.  The
+ * recurrence itself is unchanged: the pages' Eqs. (1)-(5) are sequential in t
+ * within a stream, and the segments of one stream run strictly in order.
+ *
+ *   workspace        device memory the call uses for per-stream progress
+ *                    counters (zeroed by the call on `stream`); at least
+ *                    srwm_forward_workspace_bytes(B, H) bytes, 16-byte aligned,
+ *                    owned by the caller, not overlapping any other argument.
+ *   workspace_bytes  its size.
+ * Calls that share a workspace must not overlap in time on the GPU.
+ * Other arguments, rules and return values as srwm_forward; additionally
+ * SRWM_ERR_SHAPE if the workspace is too small.
+ */
+size_t srwm_forward_workspace_bytes(int B, int H);
+int srwm_forward_balanced(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
+                          int softmax_input, float* y_out, float* W_final, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /*
  * srwm_forward_from -- srwm_forward from a per-sequence state instead of the
@@ -129,6 +156,13 @@ int srwm_set_wait_limit_ns(long long limit_ns);
  * srwm_last_device_status.  Not for production use.
  */
 int srwm_debug_skip_x_chunk(int chunk);
+
+/*
+ * srwm_debug_set_segment_len -- tests only: force the segment length (a
+ * positive multiple of 32 steps) that srwm_forward_balanced uses; 0 restores
+ * the automatic choice.  Returns SRWM_ERR_SHAPE for other values.
+ */
+int srwm_debug_set_segment_len(int steps);
 
 /*
  * srwm_probe_fma -- calibration kernel for the FP32 FMA roofline: `blocks` CTAs

@@ -7,7 +7,7 @@ names.  `inputs` holds the seeded synthetic workloads.  The binding is loaded
 on first use, so `import self_referential_weight_gb300.inputs` needs no GPU.
 """
 
-__all__ = ["srwm_forward", "srwm_forward_from", "srwm_step", "srwm_status_string", "SrwmError", "library_path"]
+__all__ = ["srwm_forward", "srwm_forward_balanced", "srwm_forward_workspace_bytes", "srwm_forward_from", "srwm_step", "srwm_status_string", "SrwmError", "library_path"]
 
 
 def __getattr__(name):

@@ -18,8 +18,9 @@ _LIB = None
 SRWM_OK = 0
 SRWM_ERR_TIMEOUT = 7
 
-EXPORTS = ("srwm_forward", "srwm_forward_from", "srwm_step", "srwm_status_string", "srwm_last_device_status",
-           "srwm_set_wait_limit_ns", "srwm_debug_skip_x_chunk", "srwm_probe_fma")
+EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_workspace_bytes", "srwm_forward_from",
+           "srwm_step", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
+           "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
 
 
 class SrwmError(RuntimeError):
@@ -45,6 +46,13 @@ def _lib():
         P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
         lib.srwm_forward.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward.restype = I
+        SZ = ctypes.c_size_t
+        lib.srwm_forward_balanced.argtypes = [P, P, I, I, I, I, I, I, P, P, P, SZ, P]
+        lib.srwm_forward_balanced.restype = I
+        lib.srwm_forward_workspace_bytes.argtypes = [I, I]
+        lib.srwm_forward_workspace_bytes.restype = SZ
+        lib.srwm_debug_set_segment_len.argtypes = [I]
+        lib.srwm_debug_set_segment_len.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward_from.restype = I
         lib.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
@@ -110,6 +118,41 @@ def srwm_forward(x, W0, n_lr, softmax_input=False, y_out=None, W_final=None, str
                              _stream_handle(stream))
     _check(rc, "srwm_forward")
     return y_out, W_final
+
+
+def srwm_forward_workspace_bytes(B, H) -> int:
+    return int(_lib().srwm_forward_workspace_bytes(int(B), int(H)))
+
+
+def srwm_forward_balanced(x, W0, n_lr, softmax_input=False, y_out=None, W_final=None, workspace=None,
+                          stream=None):
+    """srwm_forward on the load-balanced segment schedule (same results).
+
+    workspace: a CUDA tensor of at least srwm_forward_workspace_bytes(B, H)
+    bytes (allocated here when not given)."""
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    if y_out is None:
+        y_out = torch.empty((B, T, H, d), dtype=torch.float32, device=x.device)
+    if W_final is None:
+        W_final = torch.empty((B, H, m, d), dtype=torch.float32, device=W0.device)
+    nbytes = srwm_forward_workspace_bytes(B, H)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = _lib().srwm_forward_balanced(_dev(x, "x"), _dev(W0, "W0", (H, m, d)), B, T, H, d, int(n_lr),
+                                      int(bool(softmax_input)), _dev(y_out, "y_out", (B, T, H, d)),
+                                      _dev(W_final, "W_final", (B, H, m, d)),
+                                      ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(ws_bytes),
+                                      _stream_handle(stream))
+    _check(rc, "srwm_forward_balanced")
+    return y_out, W_final
+
+
+def srwm_debug_set_segment_len(steps: int) -> None:
+    _check(_lib().srwm_debug_set_segment_len(int(steps)), "srwm_debug_set_segment_len")
 
 
 def srwm_forward_from(x, W_init, n_lr, softmax_input=False, y_out=None, W_final=None, stream=None):

@@ -19,6 +19,7 @@ __device__ unsigned int g_status_word;
 
 std::atomic<long long> g_wait_limit_ns{1000000000LL};
 std::atomic<int> g_skip_chunk{-1};
+std::atomic<int> g_force_seg_len{0};
 
 constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices];
@@ -132,31 +133,78 @@ int check_params(int B, int T, int H, int d, int n_lr, int softmax_input)
     return SRWM_OK;
 }
 
-int launch(const srwm::LaunchInfo& li, const CUtensorMap& tx, const CUtensorMap& ty,
-           const srwm::KParams& kp, long long pairs, cudaStream_t stream)
+int set_smem_attr(const srwm::LaunchInfo& li)
 {
-    if (li.smem_bytes > 48 * 1024) {
-        if (cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 li.smem_bytes) != cudaSuccess) {
-            cudaGetLastError();
-            return SRWM_ERR_CUDA;
-        }
-    }
-    const dim3 grid(static_cast<unsigned>(srwm::cdiv(static_cast<int>(pairs), li.streams_per_cta)));
-    const dim3 block(static_cast<unsigned>(li.threads));
-    void* args[] = {const_cast<CUtensorMap*>(&tx), const_cast<CUtensorMap*>(&ty),
-                    const_cast<srwm::KParams*>(&kp)};
-    if (cudaLaunchKernel(li.kernel, grid, block, args, static_cast<size_t>(li.smem_bytes), stream) !=
-        cudaSuccess) {
+    if (li.smem_bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, li.smem_bytes) !=
+            cudaSuccess) {
         cudaGetLastError();
         return SRWM_ERR_CUDA;
     }
     return SRWM_OK;
 }
 
+// grid_ctas <= 0: one CTA per group of streams_per_cta streams (plain launch);
+// else a cooperative launch of exactly grid_ctas CTAs.
+int launch(const srwm::LaunchInfo& li, const CUtensorMap& tx, const CUtensorMap& ty,
+           const srwm::KParams& kp, long long pairs, int grid_ctas, cudaStream_t stream)
+{
+    int rc = set_smem_attr(li);
+    if (rc != SRWM_OK) return rc;
+    const bool coop = grid_ctas > 0;
+    const dim3 grid(static_cast<unsigned>(
+        coop ? grid_ctas : srwm::cdiv(static_cast<int>(pairs), li.streams_per_cta)));
+    const dim3 block(static_cast<unsigned>(li.threads));
+    void* args[] = {const_cast<CUtensorMap*>(&tx), const_cast<CUtensorMap*>(&ty),
+                    const_cast<srwm::KParams*>(&kp)};
+    const cudaError_t e =
+        coop ? cudaLaunchCooperativeKernel(li.kernel, grid, block, args, static_cast<size_t>(li.smem_bytes), stream)
+             : cudaLaunchKernel(li.kernel, grid, block, args, static_cast<size_t>(li.smem_bytes), stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return SRWM_OK;
+}
+
+// Co-resident CTAs of this kernel on the current device (0 on failure).
+int resident_ctas(const srwm::LaunchInfo& li)
+{
+    int dev = 0, n_sm = 0, per_sm = 0;
+    if (set_smem_attr(li) != SRWM_OK || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, li.kernel, li.threads,
+                                                      static_cast<size_t>(li.smem_bytes)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n_sm * per_sm;
+}
+
+// Segment length for the balanced schedule: a multiple of 32 steps (every
+// kernel's TMA chunk divides it) minimising rounds * (steps + reload cost),
+// where a round is one item on every slot.
+int choose_seg_len(long long n_streams, int T, long long slots)
+{
+    constexpr int kReloadSteps = 8;   // state reload, TMA refill, first read-out
+    int best_len = T;
+    double best = static_cast<double>((n_streams + slots - 1) / slots) * (T + kReloadSteps);
+    for (int len = 32; len < T; len += 32) {
+        const long long segs = (T + len - 1) / len;
+        const long long rounds = (n_streams * segs + slots - 1) / slots;
+        const double cost = static_cast<double>(rounds) * (len + kReloadSteps);
+        if (cost < best) {
+            best = cost;
+            best_len = len;
+        }
+    }
+    return best_len;
+}
+
 // Shared body of srwm_forward (per_seq = 0) and srwm_step (per_seq = 1, T = 1).
 int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, int d, int n_lr,
-        int smx, float* y, float* W_out, cudaStream_t stream)
+        int smx, float* y, float* W_out, cudaStream_t stream, int* seg_done = nullptr,
+        size_t seg_done_bytes = 0)
 {
     const long long m = 3LL * d + n_lr;
     const size_t nx = static_cast<size_t>(B) * T * H * d * sizeof(float);
@@ -198,7 +246,37 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
     kp.H = H;
     kp.w_per_seq = per_seq;
     kp.skip_chunk = g_skip_chunk.load();
-    return launch(li, tx, ty, kp, static_cast<long long>(B) * H, stream);
+    const long long pairs = static_cast<long long>(B) * H;
+    kp.n_streams = static_cast<int>(pairs);
+    kp.seg_len = T > 0 ? T : 1;
+    kp.n_items = kp.n_streams;
+    kp.seg_done = nullptr;
+    if (!seg_done) return launch(li, tx, ty, kp, pairs, 0, stream);
+
+    // Balanced schedule: streams cut into segments, a persistent cooperative
+    // grid takes (stream, segment) items in segment-major order.
+    const int ctas = resident_ctas(li);
+    if (ctas <= 0) return SRWM_ERR_CUDA;
+    const long long slots = static_cast<long long>(ctas) * li.streams_per_cta;
+    int len = g_force_seg_len.load();
+    if (len <= 0) {
+        // Nothing to balance when every stream has a slot of its own: the plain
+        // launch (one stream per slot, spread over the SMs) is the fast one.
+        if (pairs <= slots) return launch(li, tx, ty, kp, pairs, 0, stream);
+        len = choose_seg_len(pairs, T, slots);
+    }
+    if (T <= 0 || len >= T) len = T > 0 ? T : 1;
+    const long long segs = T > 0 ? (T + len - 1) / len : 1;
+    if (pairs * segs > (1LL << 31) - 1) return SRWM_ERR_SHAPE;
+    kp.seg_len = len;
+    kp.n_items = static_cast<int>(pairs * segs);
+    if (cudaMemsetAsync(seg_done, 0, seg_done_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    kp.seg_done = seg_done;
+    const long long need = (kp.n_items + li.streams_per_cta - 1) / li.streams_per_cta;
+    return launch(li, tx, ty, kp, pairs, static_cast<int>(need < ctas ? need : ctas), stream);
 }
 
 }  // namespace
@@ -213,6 +291,43 @@ int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, in
     if (rc != SRWM_OK) return rc;
     return run(x, W0, 0, B, T, H, d, n_lr, softmax_input, y_out, W_final,
                static_cast<cudaStream_t>(stream));
+}
+
+size_t srwm_forward_workspace_bytes(int B, int H)
+{
+    if (B <= 0 || H <= 0) return 0;
+    const size_t n = static_cast<size_t>(B) * static_cast<size_t>(H) * sizeof(int);
+    return (n + 255) / 256 * 256;
+}
+
+int srwm_forward_balanced(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
+                          int softmax_input, float* y_out, float* W_final, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    if (!W0 || !W_final || !workspace || (T > 0 && (!x || !y_out))) return SRWM_ERR_NULL;
+    const int rc = check_params(B, T, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    const size_t need = static_cast<size_t>(B) * H * sizeof(int);
+    if (workspace_bytes < need) return SRWM_ERR_SHAPE;
+    if (!aligned16(workspace)) return SRWM_ERR_ALIGN;
+    const long long m = 3LL * d + n_lr;
+    const size_t nx = static_cast<size_t>(B) * T * H * d * sizeof(float);
+    const size_t nw0 = static_cast<size_t>(H) * m * d * sizeof(float);
+    const size_t nwf = static_cast<size_t>(B) * H * m * d * sizeof(float);
+    if (overlaps(workspace, need, x, nx) || overlaps(workspace, need, W0, nw0) ||
+        overlaps(workspace, need, y_out, nx) || overlaps(workspace, need, W_final, nwf))
+        return SRWM_ERR_ALIAS;
+    const int prc = check_device_ptr(workspace);
+    if (prc != SRWM_OK) return prc;
+    return run(x, W0, 0, B, T, H, d, n_lr, softmax_input, y_out, W_final,
+               static_cast<cudaStream_t>(stream), static_cast<int*>(workspace), need);
+}
+
+int srwm_debug_set_segment_len(int steps)
+{
+    if (steps != 0 && (steps < 0 || steps % 32 != 0)) return SRWM_ERR_SHAPE;
+    g_force_seg_len.store(steps);
+    return SRWM_OK;
 }
 
 int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, int d, int n_lr,

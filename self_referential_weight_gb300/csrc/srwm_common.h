@@ -24,6 +24,17 @@ struct KParams {
     int B, T, H;
     int w_per_seq;                     // 1: W_init is per sequence
     int skip_chunk;                    // fault injection: x chunk not loaded (-1: none)
+    // Work items: every stream's T steps are cut into segments of seg_len
+    // steps (a multiple of each kernel's TMA chunk; seg_len >= T means one
+    // segment).  Item j is segment j / n_streams of stream j % n_streams, and a
+    // CTA (d = 64) or warp (d = 16, 32) takes items slot, slot + n_slots, ...
+    int n_streams;                     // B * H
+    int seg_len;                       // steps per item
+    int n_items;                       // n_streams * segments
+    // Per-stream count of finished segments (only when streams span several
+    // segments; NULL otherwise).  Segment s of a stream waits until its count
+    // reaches s; its state comes from W_out, where segment s - 1 left it.
+    int* seg_done;
 };
 
 // What the host needs to launch one template instantiation.

@@ -210,188 +210,220 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     constexpr int SLOTS = C::SLOTS, RG = C::RG, XW = C::XW;
     constexpr int M = 3 * D + NLR;
     constexpr int S1 = SLOTS + 1;
+    constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
     extern __shared__ unsigned char smem_raw[];
     Smem<NW>& sm = *reinterpret_cast<Smem<NW>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 2, cg = tid & 3;
-    const bool has_beta = (warp == 0);   // warp-uniform: slot 6 = row 192 + rg
-    const int p = blockIdx.x;
-    const int b = p / kp.H, h = p - b * kp.H;
-    const int T = kp.T;
-    const int nchunks = cdiv(T, TAU);
-
-    // ---- W -> registers
-    float2 w[S1][NP];
-    {
-        const float* Ws = kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * M * D;
-#pragma unroll
-        for (int i = 0; i < S1; ++i) {
-            const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
-            const bool ok = (i < SLOTS) || (has_beta && r < M);
-#pragma unroll
-            for (int j = 0; j < NP / 2; ++j) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (ok) v = __ldg(reinterpret_cast<const float4*>(Ws + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
-                w[i][2 * j] = make_float2(v.x, v.y);
-                w[i][2 * j + 1] = make_float2(v.z, v.w);
-            }
-        }
-    }
+    const bool has_beta = (warp == 0);   // warp-uniform: slot SLOTS = row 192 + rg
 
     if (tid == 0) {
         mbar_init(&sm.xbar[0], 1);
         mbar_init(&sm.xbar[1], 1);
         fence_mbar_init();
-        if (T > 0) {
+        if (kp.T > 0) {
             prefetch_tensormap(&tmx);
             prefetch_tensormap(&tmy);
         }
     }
     __syncthreads();
 
-    // ---- x staging (warp XW) and its TMA bookkeeping
-    int issued = -1, landed = -1;
-    constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
-    auto issue_chunk = [&](int c) {
-        if (lane == 0 && c != kp.skip_chunk) {
-            mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
-            tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, c * TAU, b);
-        }
-        issued = c;
-    };
-    auto stage_x = [&](int tn, float* dst) {
-        float v0 = 0.f, v1 = 0.f;
-        if (tn < T) {
-            const float* src = sm.xring[(tn / TAU) & 1][tn % TAU];
-            v0 = src[lane];
-            v1 = src[lane + 32];
-            if constexpr (SMX) softmax64(v0, v1, v0, v1);
-        }
-        dst[lane] = v0;
-        dst[lane + 32] = v1;
-    };
+    // completed phases of the two x buffers over all items of this CTA
+    uint32_t used0 = 0, used1 = 0;
+    int abort = 0;
+    int issued = -1, landed = -1;   // chunks of the current item (warp XW)
 
-    int fail = 0;
-    if (warp == XW && T > 0) {
-        issue_chunk(0);
-        if (nchunks > 1) issue_chunk(1);
-        if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], 0, kp.wait_limit_ns))) {
-            landed = 0;
-            stage_x(0, sm.xs[0]);
-            stage_x(1, sm.xs[1]);
-        } else {
-            fail = 1;
-        }
-    }
-    int abort = __syncthreads_or(fail);
+    for (int item = blockIdx.x; item < kp.n_items; item += gridDim.x) {
+        const int p = item % kp.n_streams, seg = item / kp.n_streams;
+        const int b = p / kp.H, h = p - b * kp.H;
+        const int t0 = seg * kp.seg_len;
+        const int T = min(kp.seg_len, kp.T - t0);   // steps of this item
+        const int nchunks = cdiv(T, TAU);
+        issued = -1;
+        landed = -1;
 
-    // ---- prologue: z_0 = W_0 x~_0
-    if (!abort && T > 0) {
-        float2 x2[NP];
-        load_pairs(sm.xs[0], cg, x2);
-        float2 acc[S1];
-#pragma unroll
-        for (int i = 0; i < S1; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
+        // ---- the previous segment of this stream has to be finished
+        if (seg > 0) {
+            int fail = 0;
+            if (tid == 0) fail = !wait_counter_bounded(kp.seg_done + p, seg, kp.wait_limit_ns);
+            abort = __syncthreads_or(fail);
+            if (abort) break;
+        }
+
+        // ---- W -> registers (W_init for a first segment, else the state that
+        // the previous segment left in W_out; read through L2)
+        float2 w[S1][NP];
+        {
+            const float* Ws = (seg == 0) ? kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * M * D
+                                         : kp.W_out + static_cast<size_t>(p) * M * D;
 #pragma unroll
             for (int i = 0; i < S1; ++i) {
-                if (i == SLOTS && !has_beta) continue;
-                acc[i] = __ffma2_rn(w[i][q], x2[q], acc[i]);
-            }
-        }
-        float bb[S1];
+                const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
+                const bool ok = (i < SLOTS) || (has_beta && r < M);
 #pragma unroll
-        for (int i = 0; i < S1; ++i) bb[i] = acc[i].x + acc[i].y;
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-#pragma unroll
-            for (int i = 0; i < S1; ++i) bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
-        }
-#pragma unroll
-        for (int i = 0; i < S1; ++i) {
-            if ((i & 3) != cg) continue;
-            if (i < SLOTS && C::block_of_slot(i) == 0) sm.ystage[0][0][rg + RG * i] = bb[i];
-            else if (i < SLOTS) sm.z[0][rg + RG * i] = bb[i];
-            else if (has_beta && 3 * D + rg < M) sm.z[0][3 * D + rg] = bb[i];
-        }
-        fence_proxy_async_smem();
-    }
-    __syncthreads();
-
-    // the pending rank-one update (applied at the start of the next step)
-    float coef[S1];
-#pragma unroll
-    for (int i = 0; i < S1; ++i) coef[i] = 0.f;
-    float2 pkc[NP];
-#pragma unroll
-    for (int q = 0; q < NP; ++q) pkc[q] = make_float2(0.f, 0.f);
-
-    for (int t = 0; t < T && !abort; ++t) {
-        // y chunk holding y_t complete -> TMA store
-        if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
-            const int c = t / TAU;
-            tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, c * TAU, b);
-            bulk_commit();
-            bulk_wait_read<1>();
-        }
-        // Warp 0 also carries the beta rows (slot 6); a compile-time slot count
-        // keeps each role's step free of branches.
-        if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
-        else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
-
-        // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
-        fail = 0;
-        if (warp == XW) {
-            const int tn = t + 2;
-            if (tn < T && tn % TAU == 0) {
-                const int c = tn / TAU;
-                const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
-                if (__all_sync(0xffffffffu, ok)) {
-                    landed = c;
-                    if (c + 1 < nchunks) issue_chunk(c + 1);
-                } else {
-                    fail = 1;
+                for (int j = 0; j < NP / 2; ++j) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ok) v = __ldcg(reinterpret_cast<const float4*>(Ws + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
+                    w[i][2 * j] = make_float2(v.x, v.y);
+                    w[i][2 * j + 1] = make_float2(v.z, v.w);
                 }
             }
-            if (!fail) stage_x(tn, sm.xs[t & 1]);
+        }
+
+        // ---- x staging (warp XW) and its TMA bookkeeping; chunk c of this
+        // item is steps t0 + c*TAU .. and lands in buffer c & 1
+        auto parity = [&](int c) -> uint32_t { return ((c & 1) ? used1 : used0) + (c >> 1); };
+        auto issue_chunk = [&](int c) {
+            if (lane == 0 && c != kp.skip_chunk) {
+                mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
+                tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, t0 + c * TAU, b);
+            }
+            issued = c;
+        };
+        auto stage_x = [&](int tn, float* dst) {
+            float v0 = 0.f, v1 = 0.f;
+            if (tn < T) {
+                const float* src = sm.xring[(tn / TAU) & 1][tn % TAU];
+                v0 = src[lane];
+                v1 = src[lane + 32];
+                if constexpr (SMX) softmax64(v0, v1, v0, v1);
+            }
+            dst[lane] = v0;
+            dst[lane + 32] = v1;
+        };
+
+        int fail = 0;
+        if (warp == XW && T > 0) {
+            issue_chunk(0);
+            if (nchunks > 1) issue_chunk(1);
+            if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], parity(0) & 1, kp.wait_limit_ns))) {
+                landed = 0;
+                stage_x(0, sm.xs[0]);
+                stage_x(1, sm.xs[1]);
+            } else {
+                fail = 1;
+            }
         }
         abort = __syncthreads_or(fail);
+
+        // ---- prologue: z_0 = W x~_0 (y of the item's first step)
+        if (!abort && T > 0) {
+            float2 x2[NP];
+            load_pairs(sm.xs[0], cg, x2);
+            float2 acc[S1];
+#pragma unroll
+            for (int i = 0; i < S1; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+#pragma unroll
+                for (int i = 0; i < S1; ++i) {
+                    if (i == SLOTS && !has_beta) continue;
+                    acc[i] = __ffma2_rn(w[i][q], x2[q], acc[i]);
+                }
+            }
+            float bb[S1];
+#pragma unroll
+            for (int i = 0; i < S1; ++i) bb[i] = acc[i].x + acc[i].y;
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+                for (int i = 0; i < S1; ++i) bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
+            }
+#pragma unroll
+            for (int i = 0; i < S1; ++i) {
+                if ((i & 3) != cg) continue;
+                if (i < SLOTS && C::block_of_slot(i) == 0) sm.ystage[0][0][rg + RG * i] = bb[i];
+                else if (i < SLOTS) sm.z[0][rg + RG * i] = bb[i];
+                else if (has_beta && 3 * D + rg < M) sm.z[0][3 * D + rg] = bb[i];
+            }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+
+        // the pending rank-one update (applied at the start of the next step)
+        float coef[S1];
+#pragma unroll
+        for (int i = 0; i < S1; ++i) coef[i] = 0.f;
+        float2 pkc[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) pkc[q] = make_float2(0.f, 0.f);
+
+        for (int t = 0; t < T && !abort; ++t) {
+            // y chunk holding y_t complete -> TMA store
+            if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
+                const int c = t / TAU;
+                tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
+                bulk_commit();
+                bulk_wait_read<1>();
+            }
+            // Warp 0 also carries the beta rows; a compile-time slot count keeps
+            // each role's step free of branches.
+            if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
+            else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
+
+            // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
+            fail = 0;
+            if (warp == XW) {
+                const int tn = t + 2;
+                if (tn < T && tn % TAU == 0) {
+                    const int c = tn / TAU;
+                    const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c) & 1, kp.wait_limit_ns);
+                    if (__all_sync(0xffffffffu, ok)) {
+                        landed = c;
+                        if (c + 1 < nchunks) issue_chunk(c + 1);
+                    } else {
+                        fail = 1;
+                    }
+                }
+                if (!fail) stage_x(tn, sm.xs[t & 1]);
+            }
+            abort = __syncthreads_or(fail);
+        }
+
+        // ---- drain this item's y stores
+        if (warp == 0 && lane == 0) {
+            if (!abort && T > 0 && T % TAU != 0) {
+                const int c = (T - 1) / TAU;
+                tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
+                bulk_commit();
+            }
+            bulk_wait_all<0>();
+        }
+        if (abort) break;
+        used0 += (nchunks + 1) / 2;
+        used1 += nchunks / 2;
+
+        // ---- the last pending update, then the state -> W_out[b, h]
+        float* Wd = kp.W_out + static_cast<size_t>(p) * M * D;
+#pragma unroll
+        for (int i = 0; i < S1; ++i) {
+            const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
+            if (i == SLOTS && !(has_beta && r < M)) continue;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
+#pragma unroll
+            for (int j = 0; j < NP / 2; ++j) {
+                *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
+                    make_float4(w[i][2 * j].x, w[i][2 * j].y, w[i][2 * j + 1].x, w[i][2 * j + 1].y);
+            }
+        }
+        __syncthreads();   // the state is stored; shared memory is free for the next item
+        if (kp.seg_done != nullptr && tid == 0) {
+            __threadfence();
+            st_release_gpu(kp.seg_done + p, seg + 1);
+        }
     }
 
-    // ---- drain
-    if (warp == 0 && lane == 0) {
-        if (!abort && T > 0 && T % TAU != 0) {
-            const int c = (T - 1) / TAU;
-            tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, c * TAU, b);
-            bulk_commit();
+    if (abort) {
+        if (warp == XW) {
+            // every load still in flight lands before the CTA gives up its shared memory
+            for (int c = landed + 1; c <= issued; ++c) {
+                if (c == kp.skip_chunk) continue;
+                mbar_wait_bounded(&sm.xbar[c & 1], (((c & 1) ? used1 : used0) + (c >> 1)) & 1, kp.wait_limit_ns);
+            }
         }
-        bulk_wait_all<0>();
-    }
-    if (warp == XW && abort) {
-        // every load still in flight lands before the CTA gives up its shared memory
-        for (int c = landed + 1; c <= issued; ++c) {
-            if (c == kp.skip_chunk) continue;
-            mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
-        }
-        if (lane == 0) atomicOr(kp.status, kStatusTimeout);
-    }
-    if (abort) return;
-
-    // ---- the last pending update, then W_T -> W_out[b, h]
-    float* Wd = kp.W_out + static_cast<size_t>(p) * M * D;
-#pragma unroll
-    for (int i = 0; i < S1; ++i) {
-        const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
-        if (i == SLOTS && !(has_beta && r < M)) continue;
-#pragma unroll
-        for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
-#pragma unroll
-        for (int j = 0; j < NP / 2; ++j) {
-            *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
-                make_float4(w[i][2 * j].x, w[i][2 * j].y, w[i][2 * j + 1].x, w[i][2 * j + 1].y);
-        }
+        if (tid == 0) atomicOr(kp.status, kStatusTimeout);
     }
 }
 

@@ -96,31 +96,9 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
     WarpSmem<C>& sm = reinterpret_cast<WarpSmem<C>*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127))[warp];
 
-    const int p = blockIdx.x * C::PPC + warp;
-    if (p >= kp.B * kp.H) return;  // whole warp leaves; no CTA-wide barrier below
-    const int b = p / kp.H, h = p - b * kp.H;
     const int rg = lane >> 2, cg = lane & 3;
     const int col = lane & (D - 1);   // column of this lane in the softmax layout
-    const int T = kp.T;
-    const int nchunks = cdiv(T, TAU);
-
-    float w[RPT][C::CPT];
-    {
-        const float* Ws = kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * C::M * D;
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int r = rg + 8 * i;
-#pragma unroll
-            for (int j = 0; j < C::NCH; ++j) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r < C::M) v = __ldg(reinterpret_cast<const float4*>(Ws + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
-                w[i][4 * j + 0] = v.x;
-                w[i][4 * j + 1] = v.y;
-                w[i][4 * j + 2] = v.z;
-                w[i][4 * j + 3] = v.w;
-            }
-        }
-    }
+    constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
 
     if (lane == 0) {
         mbar_init(&sm.xbar[0], 1);
@@ -129,214 +107,270 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
     }
     __syncwarp();
 
-    int issued = -1, landed = -1;
-    constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
-    auto issue_chunk = [&](int c) {
-        if (lane == 0 && c != kp.skip_chunk) {
-            mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
-            tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, c * TAU, b);
-        }
-        issued = c;
-    };
-    // x~ of step tn into dst (d = 16: both halves compute, the lower one writes).
-    auto stage_x = [&](int tn, float* dst) {
-        float v = 0.f;
-        if (tn < T) {
-            v = sm.xring[(tn / TAU) & 1][tn % TAU][col];
-            if constexpr (SMX) v = softmax_lane<D>(v);
-        }
-        if (lane < D) dst[col] = v;
-    };
-
+    // completed phases of the two x buffers over all items of this warp
+    uint32_t used0 = 0, used1 = 0;
     int abort = 0;
-    if (T > 0) {
-        issue_chunk(0);
-        if (nchunks > 1) issue_chunk(1);
-        const bool ok = mbar_wait_bounded(&sm.xbar[0], 0, kp.wait_limit_ns);
-        abort = __any_sync(0xffffffffu, !ok);
-        if (!abort) {
-            landed = 0;
-            stage_x(0, sm.xs[0]);
-            stage_x(1, sm.xs[1]);
-        }
-        __syncwarp();
-    }
+    int issued = -1, landed = -1;   // chunks of the current item
 
-    // ---- prologue: z_0 = W_0 x~_0
-    if (!abort && T > 0) {
-        float bb[RPT];
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) bb[i] = 0.f;
-#pragma unroll
-        for (int j = 0; j < C::NCH; ++j) {
-            const float4 xv = ld4(&sm.xs[0][4 * (cg + 4 * j)]);
+    const int slot = blockIdx.x * C::PPC + warp;
+    const int n_slots = gridDim.x * C::PPC;
+    for (int item = slot; item < kp.n_items; item += n_slots) {
+        const int p = item % kp.n_streams, seg = item / kp.n_streams;
+        const int b = p / kp.H, h = p - b * kp.H;
+        const int t0 = seg * kp.seg_len;
+        const int T = min(kp.seg_len, kp.T - t0);   // steps of this item
+        const int nchunks = cdiv(T, TAU);
+        issued = -1;
+        landed = -1;
+
+        // ---- the previous segment of this stream has to be finished
+        if (seg > 0) {
+            int ok = 1;
+            if (lane == 0) ok = wait_counter_bounded(kp.seg_done + p, seg, kp.wait_limit_ns);
+            abort = !__shfl_sync(0xffffffffu, ok, 0);
+            if (abort) break;
+        }
+
+        // ---- W -> registers (W_init for a first segment, else the state the
+        // previous segment left in W_out; read through L2)
+        float w[RPT][C::CPT];
+        {
+            const float* Ws = (seg == 0) ? kp.W_init + static_cast<size_t>(kp.w_per_seq ? p : h) * C::M * D
+                                         : kp.W_out + static_cast<size_t>(p) * C::M * D;
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
-                bb[i] = fmaf(w[i][4 * j + 0], xv.x, bb[i]);
-                bb[i] = fmaf(w[i][4 * j + 1], xv.y, bb[i]);
-                bb[i] = fmaf(w[i][4 * j + 2], xv.z, bb[i]);
-                bb[i] = fmaf(w[i][4 * j + 3], xv.w, bb[i]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], 1);
-            bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], 2);
-        }
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            if ((i & 3) == cg) {
                 const int r = rg + 8 * i;
-                if (r < D) sm.ystage[0][0][r] = bb[i];
-                else sm.z[r] = bb[i];
-            }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-    }
-
-    for (int t = 0; t < T && !abort; ++t) {
-        // ---------------- phase A (the whole warp)
-        if (lane == 0 && (t + 1) % TAU == 0) {
-            const int c = t / TAU;
-            tma_store_4d(&tmy, &sm.ystage[c & 1][0][0], 0, h, c * TAU, b);
-            bulk_commit();
-            bulk_wait_read<1>();
-        }
-        const float pk = softmax_lane<D>(sm.z[D + col]);
-        const float pq = softmax_lane<D>(sm.z[2 * D + col]);
-        float g[4];
-        {
-            const float4 beta = ld4(&sm.z[3 * D]);
-            if constexpr (NLR == 4) {
-                g[0] = sigmoid_fast(beta.x);
-                g[1] = sigmoid_fast(beta.y);
-                g[2] = sigmoid_fast(beta.z);
-                g[3] = sigmoid_fast(beta.w);
-            } else {
-                g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
-            }
-        }
-        if (lane < D) {
-            sm.pk[col] = pk;
-            sm.pq[col] = pq;
-        }
-        {
-            const int tn = t + 2;
-            bool ok = true;
-            if (tn < T && tn % TAU == 0) {
-                const int c = tn / TAU;
-                ok = mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
-                if (__all_sync(0xffffffffu, ok)) {
-                    landed = c;
-                    if (c + 1 < nchunks) issue_chunk(c + 1);
-                } else {
-                    ok = false;
+#pragma unroll
+                for (int j = 0; j < C::NCH; ++j) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (r < C::M) v = __ldcg(reinterpret_cast<const float4*>(Ws + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
+                    w[i][4 * j + 0] = v.x;
+                    w[i][4 * j + 1] = v.y;
+                    w[i][4 * j + 2] = v.z;
+                    w[i][4 * j + 3] = v.w;
                 }
             }
-            abort = __any_sync(0xffffffffu, !ok);
-            if (abort) break;
-            stage_x(tn, sm.xs[t & 1]);
         }
-        __syncwarp();
 
-        // ---------------- phase B: one pass over W
-        {
-            const float* xn = sm.xs[(t + 1) & 1];
-            float a[RPT], bb[RPT];
+        // chunk c of this item is steps t0 + c*TAU .. and lands in buffer c & 1
+        auto parity = [&](int c) -> uint32_t { return (((c & 1) ? used1 : used0) + (c >> 1)) & 1; };
+        auto issue_chunk = [&](int c) {
+            if (lane == 0 && c != kp.skip_chunk) {
+                mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
+                tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, t0 + c * TAU, b);
+            }
+            issued = c;
+        };
+        // x~ of step tn into dst (d = 16: both halves compute, the lower one writes).
+        auto stage_x = [&](int tn, float* dst) {
+            float v = 0.f;
+            if (tn < T) {
+                v = sm.xring[(tn / TAU) & 1][tn % TAU][col];
+                if constexpr (SMX) v = softmax_lane<D>(v);
+            }
+            if (lane < D) dst[col] = v;
+        };
+
+        if (T > 0) {
+            issue_chunk(0);
+            if (nchunks > 1) issue_chunk(1);
+            const bool ok = mbar_wait_bounded(&sm.xbar[0], parity(0), kp.wait_limit_ns);
+            abort = __any_sync(0xffffffffu, !ok);
+            if (!abort) {
+                landed = 0;
+                stage_x(0, sm.xs[0]);
+                stage_x(1, sm.xs[1]);
+            }
+            __syncwarp();
+        }
+
+        // ---- prologue: z_0 = W x~_0 (y of the item's first step)
+        if (!abort && T > 0) {
+            float bb[RPT];
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) a[i] = bb[i] = 0.f;
-            float s = 0.f;   // partial phi(k_t) . x~_{t+1} over this lane's columns
-            float4 pkv[C::NCH];
+            for (int i = 0; i < RPT; ++i) bb[i] = 0.f;
 #pragma unroll
             for (int j = 0; j < C::NCH; ++j) {
-                const int c4 = 4 * (cg + 4 * j);
-                const float4 xv = ld4(xn + c4);
-                const float4 qv = ld4(sm.pq + c4);
-                pkv[j] = ld4(sm.pk + c4);
-                const float u0 = qv.x - pkv[j].x, u1 = qv.y - pkv[j].y;
-                const float u2 = qv.z - pkv[j].z, u3 = qv.w - pkv[j].w;
-                s = fmaf(pkv[j].x, xv.x, s);
-                s = fmaf(pkv[j].y, xv.y, s);
-                s = fmaf(pkv[j].z, xv.z, s);
-                s = fmaf(pkv[j].w, xv.w, s);
+                const float4 xv = ld4(&sm.xs[0][4 * (cg + 4 * j)]);
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
-                    a[i] = fmaf(w[i][4 * j + 0], u0, a[i]);
                     bb[i] = fmaf(w[i][4 * j + 0], xv.x, bb[i]);
-                    a[i] = fmaf(w[i][4 * j + 1], u1, a[i]);
                     bb[i] = fmaf(w[i][4 * j + 1], xv.y, bb[i]);
-                    a[i] = fmaf(w[i][4 * j + 2], u2, a[i]);
                     bb[i] = fmaf(w[i][4 * j + 2], xv.z, bb[i]);
-                    a[i] = fmaf(w[i][4 * j + 3], u3, a[i]);
                     bb[i] = fmaf(w[i][4 * j + 3], xv.w, bb[i]);
                 }
             }
 #pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) {
-#pragma unroll
-                for (int i = 0; i < RPT; ++i) {
-                    a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
-                    bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
-                }
-                s += __shfl_xor_sync(0xffffffffu, s, o);
+            for (int i = 0; i < RPT; ++i) {
+                bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], 1);
+                bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], 2);
             }
-            const bool write_y = (t + 1 < T);
-            const int yb = ((t + 1) / TAU) & 1, yr = (t + 1) % TAU;
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
-                const float coef = g[C::gidx(i)] * a[i];
-#pragma unroll
-                for (int j = 0; j < C::NCH; ++j) {
-                    w[i][4 * j + 0] = fmaf(coef, pkv[j].x, w[i][4 * j + 0]);
-                    w[i][4 * j + 1] = fmaf(coef, pkv[j].y, w[i][4 * j + 1]);
-                    w[i][4 * j + 2] = fmaf(coef, pkv[j].z, w[i][4 * j + 2]);
-                    w[i][4 * j + 3] = fmaf(coef, pkv[j].w, w[i][4 * j + 3]);
-                }
-                const float zr = fmaf(coef, s, bb[i]);
                 if ((i & 3) == cg) {
                     const int r = rg + 8 * i;
-                    if (r < D) {
-                        if (write_y) sm.ystage[yb][yr][r] = zr;
-                    } else {
-                        sm.z[r] = zr;
-                    }
+                    if (r < D) sm.ystage[0][0][r] = bb[i];
+                    else sm.z[r] = bb[i];
                 }
             }
-            if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        for (int t = 0; t < T && !abort; ++t) {
+            // ---------------- phase A (the whole warp)
+            if (lane == 0 && (t + 1) % TAU == 0) {
+                const int c = t / TAU;
+                tma_store_4d(&tmy, &sm.ystage[c & 1][0][0], 0, h, t0 + c * TAU, b);
+                bulk_commit();
+                bulk_wait_read<1>();
+            }
+            const float pk = softmax_lane<D>(sm.z[D + col]);
+            const float pq = softmax_lane<D>(sm.z[2 * D + col]);
+            float g[4];
+            {
+                const float4 beta = ld4(&sm.z[3 * D]);
+                if constexpr (NLR == 4) {
+                    g[0] = sigmoid_fast(beta.x);
+                    g[1] = sigmoid_fast(beta.y);
+                    g[2] = sigmoid_fast(beta.z);
+                    g[3] = sigmoid_fast(beta.w);
+                } else {
+                    g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
+                }
+            }
+            if (lane < D) {
+                sm.pk[col] = pk;
+                sm.pq[col] = pq;
+            }
+            {
+                const int tn = t + 2;
+                bool ok = true;
+                if (tn < T && tn % TAU == 0) {
+                    const int c = tn / TAU;
+                    ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c), kp.wait_limit_ns);
+                    if (__all_sync(0xffffffffu, ok)) {
+                        landed = c;
+                        if (c + 1 < nchunks) issue_chunk(c + 1);
+                    } else {
+                        ok = false;
+                    }
+                }
+                abort = __any_sync(0xffffffffu, !ok);
+                if (abort) break;
+                stage_x(tn, sm.xs[t & 1]);
+            }
+            __syncwarp();
+
+            // ---------------- phase B: one pass over W
+            {
+                const float* xn = sm.xs[(t + 1) & 1];
+                float a[RPT], bb[RPT];
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) a[i] = bb[i] = 0.f;
+                float s = 0.f;   // partial phi(k_t) . x~_{t+1} over this lane's columns
+                float4 pkv[C::NCH];
+#pragma unroll
+                for (int j = 0; j < C::NCH; ++j) {
+                    const int c4 = 4 * (cg + 4 * j);
+                    const float4 xv = ld4(xn + c4);
+                    const float4 qv = ld4(sm.pq + c4);
+                    pkv[j] = ld4(sm.pk + c4);
+                    const float u0 = qv.x - pkv[j].x, u1 = qv.y - pkv[j].y;
+                    const float u2 = qv.z - pkv[j].z, u3 = qv.w - pkv[j].w;
+                    s = fmaf(pkv[j].x, xv.x, s);
+                    s = fmaf(pkv[j].y, xv.y, s);
+                    s = fmaf(pkv[j].z, xv.z, s);
+                    s = fmaf(pkv[j].w, xv.w, s);
+#pragma unroll
+                    for (int i = 0; i < RPT; ++i) {
+                        a[i] = fmaf(w[i][4 * j + 0], u0, a[i]);
+                        bb[i] = fmaf(w[i][4 * j + 0], xv.x, bb[i]);
+                        a[i] = fmaf(w[i][4 * j + 1], u1, a[i]);
+                        bb[i] = fmaf(w[i][4 * j + 1], xv.y, bb[i]);
+                        a[i] = fmaf(w[i][4 * j + 2], u2, a[i]);
+                        bb[i] = fmaf(w[i][4 * j + 2], xv.z, bb[i]);
+                        a[i] = fmaf(w[i][4 * j + 3], u3, a[i]);
+                        bb[i] = fmaf(w[i][4 * j + 3], xv.w, bb[i]);
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+                    for (int i = 0; i < RPT; ++i) {
+                        a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
+                        bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
+                    }
+                    s += __shfl_xor_sync(0xffffffffu, s, o);
+                }
+                const bool write_y = (t + 1 < T);
+                const int yb = ((t + 1) / TAU) & 1, yr = (t + 1) % TAU;
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const float coef = g[C::gidx(i)] * a[i];
+#pragma unroll
+                    for (int j = 0; j < C::NCH; ++j) {
+                        w[i][4 * j + 0] = fmaf(coef, pkv[j].x, w[i][4 * j + 0]);
+                        w[i][4 * j + 1] = fmaf(coef, pkv[j].y, w[i][4 * j + 1]);
+                        w[i][4 * j + 2] = fmaf(coef, pkv[j].z, w[i][4 * j + 2]);
+                        w[i][4 * j + 3] = fmaf(coef, pkv[j].w, w[i][4 * j + 3]);
+                    }
+                    const float zr = fmaf(coef, s, bb[i]);
+                    if ((i & 3) == cg) {
+                        const int r = rg + 8 * i;
+                        if (r < D) {
+                            if (write_y) sm.ystage[yb][yr][r] = zr;
+                        } else {
+                            sm.z[r] = zr;
+                        }
+                    }
+                }
+                if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+            }
+            __syncwarp();
+        }
+
+        // ---- drain this item's y stores
+        if (lane == 0) {
+            if (!abort && T > 0 && T % TAU != 0) {
+                const int c = (T - 1) / TAU;
+                tma_store_4d(&tmy, &sm.ystage[c & 1][0][0], 0, h, t0 + c * TAU, b);
+                bulk_commit();
+            }
+            bulk_wait_all<0>();
         }
         __syncwarp();
-    }
+        if (abort) break;
+        used0 += (nchunks + 1) / 2;
+        used1 += nchunks / 2;
 
-    // ---- drain
-    if (lane == 0) {
-        if (!abort && T > 0 && T % TAU != 0) {
-            const int c = (T - 1) / TAU;
-            tma_store_4d(&tmy, &sm.ystage[c & 1][0][0], 0, h, c * TAU, b);
-            bulk_commit();
-        }
-        bulk_wait_all<0>();
-    }
-    if (abort) {
-        for (int c = landed + 1; c <= issued; ++c) {
-            if (c == kp.skip_chunk) continue;
-            mbar_wait_bounded(&sm.xbar[c & 1], (c >> 1) & 1, kp.wait_limit_ns);
-        }
-        if (lane == 0) atomicOr(kp.status, kStatusTimeout);
-        return;
-    }
-
-    float* Wd = kp.W_out + static_cast<size_t>(p) * C::M * D;
+        // ---- the state -> W_out[b, h]
+        float* Wd = kp.W_out + static_cast<size_t>(p) * C::M * D;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const int r = rg + 8 * i;
-        if (r < C::M) {
+        for (int i = 0; i < RPT; ++i) {
+            const int r = rg + 8 * i;
+            if (r < C::M) {
 #pragma unroll
-            for (int j = 0; j < C::NCH; ++j) {
-                *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
-                    make_float4(w[i][4 * j + 0], w[i][4 * j + 1], w[i][4 * j + 2], w[i][4 * j + 3]);
+                for (int j = 0; j < C::NCH; ++j) {
+                    *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
+                        make_float4(w[i][4 * j + 0], w[i][4 * j + 1], w[i][4 * j + 2], w[i][4 * j + 3]);
+                }
             }
         }
+        __syncwarp();
+        if (kp.seg_done != nullptr && lane == 0) {
+            __threadfence();
+            st_release_gpu(kp.seg_done + p, seg + 1);
+        }
+    }
+
+    if (abort) {
+        // every load still in flight lands before the warp gives up its buffers
+        for (int c = landed + 1; c <= issued; ++c) {
+            if (c == kp.skip_chunk) continue;
+            mbar_wait_bounded(&sm.xbar[c & 1], (((c & 1) ? used1 : used0) + (c >> 1)) & 1, kp.wait_limit_ns);
+        }
+        if (lane == 0) atomicOr(kp.status, kStatusTimeout);
     }
 }
 

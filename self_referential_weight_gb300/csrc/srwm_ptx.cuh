@@ -118,6 +118,32 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- cross-CTA counters
+__device__ __forceinline__ int ld_acquire_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *p >= target (another CTA or warp of the same cooperative grid
+// publishes it), for at most limit_ns.  Returns false when the limit ran out.
+__device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, uint64_t limit_ns)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(100);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------- reductions
 // Butterfly reductions over aligned groups of W lanes (W a power of two).
 // Every lane of a group ends with the same bits: each level adds the same two

@@ -26,7 +26,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(srwm_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(srwm_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -121,3 +121,29 @@ def test_forward_from_validation(lib):
     assert call(x=A + 4) == 4
     assert call(Wf=A + 0x1000000 + 16) == 5      # partial overlap of W_final with W_init
     assert lib.srwm_forward_from(A, A + 0x1000000, 2, 3, 2, 48, 4, 0, A + 0x2000000, A + 0x3000000, None) == 3
+
+
+def test_forward_balanced_validation(lib):
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.srwm_forward_balanced.argtypes = [P, P, I, I, I, I, I, I, P, P, P, SZ, P]
+    lib.srwm_forward_workspace_bytes.argtypes = [I, I]
+    lib.srwm_forward_workspace_bytes.restype = SZ
+    need = lib.srwm_forward_workspace_bytes(2, 2)
+    assert need >= 2 * 2 * 4 and need % 256 == 0
+    assert lib.srwm_forward_workspace_bytes(0, 2) == 0
+    ws = A + 0x4000000
+
+    def call(ws=ws, nbytes=need, **kw):
+        return lib.srwm_forward_balanced(A, A + 0x1000000, 2, 3, 2, 16, 4, 0, A + 0x2000000,
+                                         A + 0x3000000, ws, nbytes, None)
+
+    assert call(ws=None) == 1
+    assert call(nbytes=8) == 2
+    assert call(ws=ws + 4) == 4
+    assert call(ws=A + 0x2000000 + 64) == 5      # workspace inside y_out
+
+
+def test_debug_segment_len_rejects_bad_values(lib):
+    assert lib.srwm_debug_set_segment_len(33) == 2
+    assert lib.srwm_debug_set_segment_len(-32) == 2
+    assert lib.srwm_debug_set_segment_len(0) == 0

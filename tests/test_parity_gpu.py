@@ -247,3 +247,50 @@ def test_forward_from_zero_steps_copies_state():
     _, Wf = binding.srwm_forward_from(x, W, 4)
     torch.cuda.synchronize()
     assert torch.equal(Wf, W)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
+def test_balanced_forced_segments_match(d, n_lr, smx):
+    """The balanced schedule with short forced segments (32 steps, a ragged
+    last one): every stream hops between slots through W_final and the
+    progress counters.  Equals srwm_forward within fp32 rounding, matches the
+    oracle, and is deterministic."""
+    wl = inputs.Workload("t", 3, 150, 2, d, n_lr, smx, 120 + d, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
+    binding.srwm_debug_set_segment_len(32)
+    try:
+        yb, Wb = binding.srwm_forward_balanced(xd, W0d, n_lr, smx)
+        yb2, Wb2 = binding.srwm_forward_balanced(xd, W0d, n_lr, smx)
+        torch.cuda.synchronize()
+        assert binding.srwm_last_device_status() == 0
+    finally:
+        binding.srwm_debug_set_segment_len(0)
+    yb, Wb = yb.cpu().numpy(), Wb.cpu().numpy()
+    assert rel(yb, y) <= 1e-5 and rel(Wb, Wf) <= 1e-5
+    np.testing.assert_array_equal(yb, yb2.cpu().numpy())
+    np.testing.assert_array_equal(Wb, Wb2.cpu().numpy())
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    assert rel(yb, yo) <= 1e-4 and rel(Wb, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("name", ["mid", "rl", "fewshot"])
+def test_balanced_full_size_sampled(name):
+    """The balanced schedule at full size with its automatic segment length;
+    the oracle recomputes sampled streams."""
+    wl = inputs.workload(name)
+    x, W0 = inputs.make_inputs(wl)
+    yb, Wb = binding.srwm_forward_balanced(torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV),
+                                           wl.n_lr, wl.softmax_input)
+    torch.cuda.synchronize()
+    assert binding.srwm_last_device_status() == 0
+    yb, Wb = yb.cpu().numpy(), Wb.cpu().numpy()
+    rng = np.random.default_rng(1)
+    picks = {(0, 0), (wl.B - 1, wl.H - 1)}
+    while len(picks) < 8:
+        picks.add((int(rng.integers(wl.B)), int(rng.integers(wl.H))))
+    for b, h in sorted(picks):
+        yo, Wo = oracle.forward(x[b:b + 1, :, h:h + 1], W0[h:h + 1], wl.n_lr, wl.softmax_input)
+        assert rel(yb[b, :, h], yo[0, :, 0]) <= tol(wl.T) and rel(Wb[b, h], Wo[0, 0]) <= tol(wl.T)
