@@ -97,6 +97,29 @@ int srwm_forward_balanced(const float* x, const float* W0, int B, int T, int H, 
                           size_t workspace_bytes, void* stream);
 
 /*
+ * srwm_forward_balanced_noalloc -- srwm_forward_balanced without the
+ * workspace argument, for callers that cannot allocate device memory (a host
+ * framework that owns every allocation and gives plugins no allocator, or a
+ * path that must not call cudaMalloc and accept its implicit synchronisation).
+ * The pages have no counterpart to this entry point: it only changes where the
+ * schedule's scratch lives.
+ *
+ * The per-stream progress counters live in a fixed array inside the library
+ * (256 KiB on every GPU that loads it, held until the process exits), so at
+ * most 65536 streams: B * H above that returns SRWM_ERR_SHAPE before anything
+ * is enqueued.  The first call on a device looks up the array's device
+ * address; make that first call before any stream capture on that device.
+ * All calls share the one array: each call clears the counters it needs
+ * before its kernel runs, and calls that overlap in time on the GPU (on
+ * different streams, or from different host threads) race on it.
+ * Arguments and results otherwise as srwm_forward_balanced.  Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library call.
+ */
+int srwm_forward_balanced_noalloc(const float* x, const float* W0, int B, int T, int H, int d,
+                                  int n_lr, int softmax_input, float* y_out, float* W_final,
+                                  void* stream);
+
+/*
  * srwm_forward_from -- srwm_forward from a per-sequence state instead of the
  * shared W0: the state carried across truncation windows, e.g. RL rollouts
  * that keep W_t until the episode ends (review of "A Modern Self-Referential

@@ -18,7 +18,8 @@ _LIB = None
 SRWM_OK = 0
 SRWM_ERR_TIMEOUT = 7
 
-EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_workspace_bytes", "srwm_forward_from",
+EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noalloc",
+           "srwm_forward_workspace_bytes", "srwm_forward_from",
            "srwm_step", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
            "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
 
@@ -51,6 +52,8 @@ def _lib():
         lib.srwm_forward_balanced.restype = I
         lib.srwm_forward_workspace_bytes.argtypes = [I, I]
         lib.srwm_forward_workspace_bytes.restype = SZ
+        lib.srwm_forward_balanced_noalloc.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
+        lib.srwm_forward_balanced_noalloc.restype = I
         lib.srwm_debug_set_segment_len.argtypes = [I]
         lib.srwm_debug_set_segment_len.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
@@ -148,6 +151,19 @@ def srwm_forward_balanced(x, W0, n_lr, softmax_input=False, y_out=None, W_final=
                                       ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(ws_bytes),
                                       _stream_handle(stream))
     _check(rc, "srwm_forward_balanced")
+    return y_out, W_final
+
+
+def srwm_forward_balanced_noalloc(x, W0, n_lr, softmax_input, y_out, W_final, stream=None):
+    """srwm_forward_balanced with the library's own fixed scratch array instead
+    of a workspace, for callers that cannot allocate device memory.  The
+    outputs are the caller's (they must be given); B*H is at most 65536."""
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    rc = _lib().srwm_forward_balanced_noalloc(_dev(x, "x"), _dev(W0, "W0", (H, m, d)), B, T, H, d, int(n_lr),
+                                              int(bool(softmax_input)), _dev(y_out, "y_out", (B, T, H, d)),
+                                              _dev(W_final, "W_final", (B, H, m, d)), _stream_handle(stream))
+    _check(rc, "srwm_forward_balanced_noalloc")
     return y_out, W_final
 
 
