@@ -36,7 +36,7 @@ METRIC = "SRWM head-token updates/s (B*T*H/s) and % of FP32 FMA peak, 1 GB300"
 UNIT = "head-token updates/s"
 FMA_PER_CLK_PER_SM = 128          # FP32 FMA lanes per SM (4 SMSPs x 32)
 L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "srwm_cta_kernel_mid.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "srwm_d64_kernel_mid.md")
 KERNEL_SOURCES = ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"]
 
 
@@ -58,6 +58,24 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(seconds, device=None):
+    """Largest value over all ranks (the job's time is its slowest rank's);
+    the value itself when not running distributed."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(seconds)
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(wl, rank):
+    """Weak scaling: every rank runs the same workload shape on its own seed."""
+    return wl.with_shape(seed=wl.seed + 1000 * rank) if rank else wl
 
 
 def fmas_per_head_token(wl):
@@ -242,7 +260,7 @@ def main():
             dist.barrier()
 
     # per-rank data: the same workload shape, a rank-specific seed (weak scaling)
-    wl_r = wl.with_shape(seed=wl.seed + 1000 * rank) if rank else wl
+    wl_r = rank_workload(wl, rank)
     x_np, W0_np = inputs.make_inputs(wl_r)
     x = torch.from_numpy(x_np).to(dev)
     W0 = torch.from_numpy(W0_np).to(dev)
@@ -283,13 +301,7 @@ def main():
     t_dev = sum(per_step) / 1e3
     if binding.srwm_last_device_status(stream) != 0:
         raise RuntimeError("device status set during the timed region")
-    t_max = t_dev
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([t_dev], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(t_dev, dev)
 
     ht_per_step = wl.head_tokens
     value = world * ht_per_step * args.steps / t_max
@@ -321,13 +333,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
     e2e = {"value": world * ht_per_step * args.e2e_steps / t_e2e, "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * 4 + W0_h.numel() * 4,
            "d2h_bytes_per_step": y_h.numel() * 4 + Wf_h.numel() * 4,
