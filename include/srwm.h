@@ -152,6 +152,45 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
 int srwm_step(const float* x_t, const float* W_in, int B, int H, int d, int n_lr,
               int softmax_input, float* y_t, float* W_out, void* stream);
 
+/*
+ * srwm_backward -- gradients of a loss through srwm_forward: given the
+ * cotangents dy = dL/dy and (optionally) dW_final = dL/dW_final of one
+ * srwm_forward(x, W0, ...) call, writes dx = dL/dx and dW0 = dL/dW0.  The
+ * training of these models backpropagates through the whole sequence
+ * ("Metalearning Continual Learning Algorithms", section 2.3, which trains
+ * the SRWM by gradient descent through its own updates).  The derivative is
+ * taken of the exact recurrence above, including the softmaxes, the sigmoid
+ * gates and x~ = softmax(x) when softmax_input = 1.
+ *
+ *   x         [B, T, H, d]    the forward's inputs
+ *   W0        [H, m, d]       the forward's shared initial state
+ *   dy        [B, T, H, d]    dL/dy
+ *   dW_final  [B, H, m, d]    dL/dW_final, or NULL for zero
+ *   dx        [B, T, H, d]    written
+ *   dW0       [H, m, d]       written: the sum over sequences b of each
+ *                             stream's dL/dW0, summed in order of b
+ *   workspace device scratch of at least srwm_backward_workspace_bytes(...)
+ *             bytes, 16-byte aligned, contents irrelevant on entry; it holds
+ *             the state W at the start of every 32-step segment and the
+ *             per-stream dL/dW0.  It must stay untouched until the work on
+ *             `stream` has finished.
+ *
+ * The forward is recomputed inside (one extra forward pass); y and W_final
+ * are not needed.  T = 0 writes dW0 = sum_b dW_final (or zero).  The same
+ * pointer rules as above apply; the workspace must not overlap anything else.
+ * Returns SRWM_ERR_SHAPE when workspace_bytes is too small.
+ */
+int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
+                  int softmax_input, const float* dy, const float* dW_final, float* dx, float* dW0,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * srwm_backward_workspace_bytes -- scratch size srwm_backward needs for these
+ * sizes: 4 * B * H * m * d * ceil(T / 32) bytes (at least one segment),
+ * rounded up to 256.  Returns 0 for unsupported or invalid sizes.
+ */
+size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* srwm_status_string(int status);
 

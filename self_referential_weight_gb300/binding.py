@@ -20,7 +20,7 @@ SRWM_ERR_TIMEOUT = 7
 
 EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noalloc",
            "srwm_forward_workspace_bytes", "srwm_forward_from",
-           "srwm_step", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
+           "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
            "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
 
 
@@ -60,6 +60,10 @@ def _lib():
         lib.srwm_forward_from.restype = I
         lib.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
         lib.srwm_step.restype = I
+        lib.srwm_backward.argtypes = [P, P, I, I, I, I, I, I, P, P, P, P, P, SZ, P]
+        lib.srwm_backward.restype = I
+        lib.srwm_backward_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.srwm_backward_workspace_bytes.restype = SZ
         lib.srwm_status_string.argtypes = [I]
         lib.srwm_status_string.restype = ctypes.c_char_p
         lib.srwm_last_device_status.argtypes = [P]
@@ -203,6 +207,37 @@ def srwm_step(x_t, W_in, n_lr, softmax_input=False, y_t=None, W_out=None, stream
                           _dev(W_out, "W_out", (B, H, m, d)), _stream_handle(stream))
     _check(rc, "srwm_step")
     return y_t, W_out
+
+
+def srwm_backward_workspace_bytes(B, T, H, d, n_lr) -> int:
+    return int(_lib().srwm_backward_workspace_bytes(int(B), int(T), int(H), int(d), int(n_lr)))
+
+
+def srwm_backward(x, W0, n_lr, softmax_input, dy, dW_final=None, dx=None, dW0=None, workspace=None,
+                  stream=None):
+    """Gradients through srwm_forward(x, W0, ...): returns (dx [B,T,H,d], dW0 [H,m,d]).
+
+    dy [B,T,H,d] = dL/dy; dW_final [B,H,m,d] = dL/dW_final or None (zero).
+    The workspace is allocated when not given."""
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    if dx is None:
+        dx = torch.empty((B, T, H, d), dtype=torch.float32, device=x.device)
+    if dW0 is None:
+        dW0 = torch.empty((H, m, d), dtype=torch.float32, device=W0.device)
+    need = srwm_backward_workspace_bytes(B, T, H, d, n_lr)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    pf = _dev(dW_final, "dW_final", (B, H, m, d)) if dW_final is not None else ctypes.c_void_p(0)
+    rc = _lib().srwm_backward(_dev(x, "x"), _dev(W0, "W0", (H, m, d)), B, T, H, d, int(n_lr),
+                              int(bool(softmax_input)), _dev(dy, "dy", (B, T, H, d)), pf,
+                              _dev(dx, "dx", (B, T, H, d)), _dev(dW0, "dW0", (H, m, d)),
+                              ctypes.c_void_p(workspace.data_ptr()),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "srwm_backward")
+    return dx, dW0
 
 
 def srwm_last_device_status(stream=None) -> int:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsrwm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["srwm_api.cu", "srwm_d16.cu", "srwm_d32.cu", "srwm_d64.cu", "srwm_probe.cu", "srwm_noalloc.cu"]
+UNITS = ["srwm_api.cu", "srwm_d16.cu", "srwm_d32.cu", "srwm_d64.cu", "srwm_probe.cu", "srwm_noalloc.cu", "srwm_bwd.cu"]
 
 
 def _nvcc() -> str:

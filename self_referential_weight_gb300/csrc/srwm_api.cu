@@ -11,6 +11,7 @@
 
 #include "srwm.h"
 #include "srwm_common.h"
+#include "srwm_bwd.cuh"
 
 namespace {
 
@@ -328,6 +329,88 @@ int srwm_debug_set_segment_len(int steps)
     if (steps != 0 && (steps < 0 || steps % 32 != 0)) return SRWM_ERR_SHAPE;
     g_force_seg_len.store(steps);
     return SRWM_OK;
+}
+
+size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr)
+{
+    if (B <= 0 || H <= 0 || T < 0 || (d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4)) return 0;
+    const size_t md = static_cast<size_t>(3 * d + n_lr) * d;
+    const size_t streams = static_cast<size_t>(B) * H;
+    const size_t nseg = T > 0 ? static_cast<size_t>((T + 31) / 32) : 1;
+    const size_t floats = streams * md * nseg;   // dL/dW0 per stream + states of segments 1..
+    return (floats * sizeof(float) + 255) / 256 * 256;
+}
+
+int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr, int softmax_input,
+                  const float* dy, const float* dW_final, float* dx, float* dW0, void* workspace,
+                  size_t workspace_bytes, void* stream)
+{
+    if (!W0 || !dW0 || !workspace || (T > 0 && (!x || !dy || !dx))) return SRWM_ERR_NULL;
+    int rc = check_params(B, T, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return SRWM_ERR_SHAPE;   // one CTA per stream
+    const size_t need = srwm_backward_workspace_bytes(B, T, H, d, n_lr);
+    if (workspace_bytes < need) return SRWM_ERR_SHAPE;
+    const long long m = 3LL * d + n_lr;
+    const size_t nx = static_cast<size_t>(B) * T * H * d * sizeof(float);
+    const size_t nw0 = static_cast<size_t>(H) * m * d * sizeof(float);
+    const size_t nwf = static_cast<size_t>(B) * H * m * d * sizeof(float);
+    if (!aligned16(W0) || !aligned16(dW0) || !aligned16(workspace) || (dW_final && !aligned16(dW_final)) ||
+        (T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
+        return SRWM_ERR_ALIGN;
+    const void* ins[4] = {x, W0, dy, dW_final};
+    const size_t in_bytes[4] = {nx, nw0, nx, nwf};
+    for (int i = 0; i < 4; ++i) {
+        if (overlaps(dx, nx, ins[i], in_bytes[i]) || overlaps(dW0, nw0, ins[i], in_bytes[i]) ||
+            overlaps(workspace, need, ins[i], in_bytes[i]))
+            return SRWM_ERR_ALIAS;
+    }
+    if (overlaps(dx, nx, dW0, nw0) || overlaps(dx, nx, workspace, need) || overlaps(dW0, nw0, workspace, need))
+        return SRWM_ERR_ALIAS;
+    const void* devs[8] = {W0, dW0, workspace, dW_final, x, dy, dx, nullptr};
+    for (int i = 0; i < 7; ++i) {
+        if (!devs[i] || (i >= 4 && T == 0)) continue;
+        if ((rc = check_device_ptr(devs[i])) != SRWM_OK) return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* dW_seq = static_cast<float*>(workspace);
+    const size_t per_batch = static_cast<size_t>(H) * m * d;
+    if (T == 0) {
+        // dL/dW0 = sum over b of dL/dW_final (W_final = W0 for every b)
+        if (!dW_final) {
+            if (cudaMemsetAsync(dW0, 0, nw0, st) != cudaSuccess) {
+                cudaGetLastError();
+                return SRWM_ERR_CUDA;
+            }
+            return SRWM_OK;
+        }
+        return srwm::launch_sum_over_batch(dW_final, dW0, B, per_batch, st) == 0 ? SRWM_OK : SRWM_ERR_CUDA;
+    }
+    const srwm::BwdLaunch li = srwm::bwd_info(d, n_lr);
+    if (cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, li.smem_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    srwm::BwdParams bp;
+    bp.x = x;
+    bp.W0 = W0;
+    bp.dy = dy;
+    bp.dWf = dW_final;
+    bp.dx = dx;
+    bp.dW_seq = dW_seq;
+    bp.snap = dW_seq + static_cast<size_t>(B) * per_batch;
+    bp.B = B;
+    bp.T = T;
+    bp.H = H;
+    int smx = softmax_input;
+    void* args[] = {&bp, &smx};
+    if (cudaLaunchKernel(li.kernel, dim3(static_cast<unsigned>(static_cast<long long>(B) * H)),
+                         dim3(static_cast<unsigned>(li.threads)), args, static_cast<size_t>(li.smem_bytes),
+                         st) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return srwm::launch_sum_over_batch(dW_seq, dW0, B, per_batch, st) == 0 ? SRWM_OK : SRWM_ERR_CUDA;
 }
 
 int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, int d, int n_lr,

@@ -1,0 +1,418 @@
+// srwm_bwd.cuh -- backward pass of the SRWM recurrence (gradients of a loss
+// L(y, W_final) with respect to x and W0), one CTA per (sequence, head)
+// stream, W and dL/dW both held in registers.
+//
+// Forward ("Metalearning Continual Learning Algorithms", section 2.3,
+// Eqs. (1)-(5)), per step t with x~ = x or softmax(x):
+//   z = W x~;  y = z[0:d];  pk = phi(z[d:2d]);  pq = phi(z[2d:3d]);  g = sigmoid(beta)
+//   u = pq - pk;  a = W u;  coef_r = g_blk(r) a_r;  W' = W + coef (outer) pk
+// Backward through one step, from dW' = dL/dW' and dy:
+//   W      = W' - coef (outer) pk                  (the recorded update, subtracted)
+//   dcoef  = dW' pk;   da = g dcoef;   dg_blk = sum_{r in blk} dcoef_r a_r
+//   dpk    = dW'^T coef - W^T da;   dpq = W^T da
+//   dk     = pk (dpk - <pk, dpk>);  dq = pq (dpq - <pq, dpq>);  dbeta = dg g (1 - g)
+//   dz     = [dy, dk, dq, dbeta];   dx~ = W^T dz
+//   dW     = dW' + da (outer) u + dz (outer) x~
+// (and dx = x~ (dx~ - <x~, dx~>) when the input goes through softmax).
+//
+// Memory: the pages name "memory-efficient" backpropagation through time
+// without details.  Here the state W is kept only at the start of every
+// KSEG-step segment (phase 1 recomputes the forward once and stores those
+// states in the workspace); phase 2 walks the segments backwards, recomputes
+// each one from its stored start, records per step phi(k), u, the gates, a and
+// x~ in shared memory, and then steps back through it.  Stepping back
+// subtracts exactly the update that the recompute added, so no matrix
+// inversion (which would amplify rounding wherever the update contracts W) is
+// needed, and rounding cannot accumulate past one segment.
+//
+// Layout: thread (rg = tid/4, cg = tid%4) holds rows rg + RG i (i < S) and the
+// D/4 columns of float4 chunks cg + 4 j.  Row dot products finish with two xor
+// shuffles over the four column groups; column sums over rows finish with a
+// transposed butterfly over the eight row groups of a warp and a fixed-order
+// sum over warps in shared memory, so the result is deterministic.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "srwm_common.h"
+#include "srwm_ptx.cuh"
+
+namespace srwm {
+
+struct BwdParams {
+    const float* x;        // [B, T, H, D]
+    const float* W0;       // [H, M, D]
+    const float* dy;       // [B, T, H, D]
+    const float* dWf;      // [B, H, M, D] or nullptr (zero)
+    float* dx;             // [B, T, H, D]
+    float* dW_seq;         // [B, H, M, D]: dL/dW0 of every stream (summed over b later)
+    float* snap;           // [B * H][n_seg - 1][M * D]: W at the start of segments 1..
+    int B, T, H;
+};
+
+template <int D_, int NLR_>
+struct BwdCfg {
+    static constexpr int D = D_, NLR = NLR_;
+    static constexpr int M = 3 * D + NLR;
+    static constexpr int NW = D == 64 ? 8 : (D == 32 ? 4 : 2);
+    static constexpr int NT = 32 * NW;
+    static constexpr int RG = 8 * NW;            // row groups
+    static constexpr int S = cdiv(M, RG);        // row slots per thread
+    static constexpr int MP = S * RG;            // padded rows
+    static constexpr int CPT = D / 4;            // columns per thread
+    static constexpr int NCH = CPT / 4;          // float4 chunks per thread
+    static constexpr int KSEG = 32;              // steps per segment
+    static constexpr int NV2 = 2 * CPT;          // values of a two-vector column reduction
+    static constexpr int NV1 = CPT < 8 ? 8 : CPT;  // one-vector reduction (padded to 8)
+};
+
+template <class C>
+struct __align__(16) BwdSmem {
+    float xs[C::KSEG][C::D];   // x~ of the segment's steps
+    float dyv[C::KSEG][C::D];  // dy of the segment's steps
+    float pk[C::KSEG][C::D];
+    float u[C::KSEG][C::D];
+    float a[C::KSEG][C::MP];
+    float g[C::KSEG][4];
+    float z[C::MP];
+    float dz[C::MP];
+    float dgrow[C::MP];
+    float red[C::NW][2][C::D];   // per-warp column partials
+    float vec[2][C::D];          // column sums
+};
+
+template <class C>
+__device__ __forceinline__ int bcol(int cg, int q) { return 4 * (cg + 4 * (q >> 2)) + (q & 3); }
+
+// Transposed butterfly over the 8 row groups of a warp (lanes with equal
+// lane%4): afterwards lane holds in v[0 .. N/8) the sums of the entries
+// rg_lo*N/8 .. rg_lo*N/8 + N/8 - 1, where rg_lo = (lane / 4) % 8.
+template <int N>
+__device__ __forceinline__ void rowgroup_reduce(float (&v)[N], int lane)
+{
+    static_assert(N % 8 == 0, "N must be a multiple of 8");
+#pragma unroll
+    for (int lvl = 0; lvl < 3; ++lvl) {
+        const int mask = 16 >> lvl;
+        const int half = N >> (lvl + 1);
+        const bool hi = (lane & mask) != 0;
+#pragma unroll
+        for (int e = 0; e < half; ++e) {
+            const float send = hi ? v[e] : v[e + half];
+            const float keep = hi ? v[e + half] : v[e];
+            v[e] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+}
+
+// softmax over the D values in[0..D) by one warp; writes out[0..D).
+template <int D>
+__device__ __forceinline__ void warp_softmax(const float* in, float* out, int lane)
+{
+    if constexpr (D == 64) {
+        float p0, p1;
+        softmax64(in[lane], in[lane + 32], p0, p1);
+        out[lane] = p0;
+        out[lane + 32] = p1;
+    } else {
+        const int c = lane & (D - 1);
+        const float mx = redux_max(in[c]);
+        const float e = __expf(in[c] - mx);
+        float sum = warp_sum_unit1(e);
+        if constexpr (D == 16) sum *= 0.5f;
+        if (lane < D) out[c] = e * rcp_approx(sum);
+    }
+}
+
+// softmax backward over D values by one warp: out = s (gin - <s, gin>).
+template <int D>
+__device__ __forceinline__ void warp_softmax_bwd(const float* s, const float* gin, float* out, int lane)
+{
+    float dot = 0.f;
+    for (int c = lane; c < D; c += 32) dot = fmaf(s[c], gin[c], dot);
+    dot = group_sum<32>(dot);
+    for (int c = lane; c < D; c += 32) out[c] = s[c] * (gin[c] - dot);
+}
+
+template <int D, int NLR>
+__global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
+    srwm_bwd_kernel(const BwdParams bp, int softmax_input)
+{
+    using C = BwdCfg<D, NLR>;
+    constexpr int M = C::M, S = C::S, RG = C::RG, CPT = C::CPT, KSEG = C::KSEG;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<C>& sm = *reinterpret_cast<BwdSmem<C>*>(smem_raw);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rg = tid >> 2, cg = tid & 3;
+    const int p = blockIdx.x;
+    const int b = p / bp.H, h = p - b * bp.H;
+    const int T = bp.T;
+    const int nseg = cdiv(T, KSEG);
+    const size_t MD = static_cast<size_t>(M) * D;
+    auto blk = [](int r) { return NLR == 1 ? 0 : (r < 3 * D ? r / D : 3); };
+    auto gidx = [&](int r) { return blk(r); };
+
+    float w[S][CPT], dw[S][CPT];
+
+    auto load_state = [&](const float* src) {
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            const int r = rg + RG * i;
+#pragma unroll
+            for (int j = 0; j < C::NCH; ++j) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < M) v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
+                w[i][4 * j + 0] = v.x;
+                w[i][4 * j + 1] = v.y;
+                w[i][4 * j + 2] = v.z;
+                w[i][4 * j + 3] = v.w;
+            }
+        }
+    };
+    auto store_tile = [&](float (&m)[S][CPT], float* dst) {
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            const int r = rg + RG * i;
+            if (r >= M) continue;
+#pragma unroll
+            for (int j = 0; j < C::NCH; ++j)
+                *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
+                    make_float4(m[i][4 * j + 0], m[i][4 * j + 1], m[i][4 * j + 2], m[i][4 * j + 3]);
+        }
+    };
+    // x~ (and optionally dy) of steps t0 .. t0+len-1 into shared memory
+    auto stage = [&](int t0, int len, bool with_dy) {
+        for (int idx = tid; idx < len * D; idx += C::NT) {
+            const int s = idx / D, c = idx - s * D;
+            const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D + c;
+            sm.xs[s][c] = bp.x[g];
+            if (with_dy) sm.dyv[s][c] = bp.dy[g];
+        }
+        __syncthreads();
+        if (softmax_input) {
+            for (int s = warp; s < len; s += C::NW) warp_softmax<D>(sm.xs[s], sm.xs[s], lane);
+            __syncthreads();
+        }
+    };
+    // one forward step (local index s) on the register tile, recording
+    // phi(k), u, gates and a
+    auto fwd_step = [&](int s) {
+        float zp[S];
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            zp[i] = 0.f;
+#pragma unroll
+            for (int q = 0; q < CPT; ++q) zp[i] = fmaf(w[i][q], sm.xs[s][bcol<C>(cg, q)], zp[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            zp[i] += __shfl_xor_sync(0xffffffffu, zp[i], 1);
+            zp[i] += __shfl_xor_sync(0xffffffffu, zp[i], 2);
+            if ((i & 3) == cg) sm.z[rg + RG * i] = zp[i];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            warp_softmax<D>(sm.z + D, sm.pk[s], lane);
+            warp_softmax<D>(sm.z + 2 * D, sm.u[s], lane);   // phi(q) for now
+            if (lane < 4) sm.g[s][lane] = sigmoid_fast(sm.z[3 * D + (NLR == 4 ? lane : 0)]);
+            __syncwarp();
+            for (int c = lane; c < D; c += 32) sm.u[s][c] -= sm.pk[s][c];
+        }
+        __syncthreads();
+        float ap[S];
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            ap[i] = 0.f;
+#pragma unroll
+            for (int q = 0; q < CPT; ++q) ap[i] = fmaf(w[i][q], sm.u[s][bcol<C>(cg, q)], ap[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            ap[i] += __shfl_xor_sync(0xffffffffu, ap[i], 1);
+            ap[i] += __shfl_xor_sync(0xffffffffu, ap[i], 2);
+            const int r = rg + RG * i;
+            if ((i & 3) == cg) sm.a[s][r] = ap[i];
+            const float coef = sm.g[s][gidx(r)] * ap[i];
+#pragma unroll
+            for (int q = 0; q < CPT; ++q) w[i][q] = fmaf(coef, sm.pk[s][bcol<C>(cg, q)], w[i][q]);
+        }
+    };
+    // column sums over all rows of per-thread partials v[N] (N/CPT vectors):
+    // afterwards sm.vec[vv][c] holds vector vv at column c
+    auto colsum = [&](auto& v, int nvec) {
+        constexpr int N = sizeof(v) / sizeof(float);
+        rowgroup_reduce<N>(v, lane);
+        const int rg_lo = (lane >> 2) & 7;
+#pragma unroll
+        for (int e = 0; e < N / 8; ++e) {
+            const int idx = rg_lo * (N / 8) + e;
+            const int vv = idx / CPT, q = idx - vv * CPT;
+            if (vv < nvec) sm.red[warp][vv][bcol<C>(cg, q)] = v[e];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nvec * D; idx += C::NT) {
+            const int vv = idx / D, c = idx - vv * D;
+            float acc = 0.f;
+            for (int ww = 0; ww < C::NW; ++ww) acc += sm.red[ww][vv][c];
+            sm.vec[vv][c] = acc;
+        }
+        __syncthreads();
+    };
+
+    // ---- phase 1: states at the start of segments 1 .. nseg-1
+    load_state(bp.W0 + static_cast<size_t>(h) * MD);
+    for (int j = 0; j + 1 < nseg; ++j) {
+        stage(j * KSEG, KSEG, false);
+        for (int s = 0; s < KSEG; ++s) {
+            fwd_step(s);
+            __syncthreads();
+        }
+        store_tile(w, bp.snap + (static_cast<size_t>(p) * (nseg - 1) + j) * MD);
+    }
+
+    // ---- phase 2: segments backwards
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+        const int r = rg + RG * i;
+#pragma unroll
+        for (int j = 0; j < C::NCH; ++j) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (bp.dWf != nullptr && r < M)
+                v = *reinterpret_cast<const float4*>(bp.dWf + static_cast<size_t>(p) * MD + static_cast<size_t>(r) * D + 4 * (cg + 4 * j));
+            dw[i][4 * j + 0] = v.x;
+            dw[i][4 * j + 1] = v.y;
+            dw[i][4 * j + 2] = v.z;
+            dw[i][4 * j + 3] = v.w;
+        }
+    }
+    __syncthreads();   // every thread is done writing the last snapshot
+    for (int j = nseg - 1; j >= 0; --j) {
+        const int t0 = j * KSEG;
+        const int len = min(KSEG, T - t0);
+        if (j == 0) load_state(bp.W0 + static_cast<size_t>(h) * MD);
+        else load_state(bp.snap + (static_cast<size_t>(p) * (nseg - 1) + (j - 1)) * MD);
+        stage(t0, len, true);
+        for (int s = 0; s < len; ++s) {
+            fwd_step(s);
+            __syncthreads();
+        }
+        for (int s = len - 1; s >= 0; --s) {
+            // 1. step back: W_{t-1} = W_t - coef (outer) pk; dcoef = dW pk
+            float av[S], dco[S];
+#pragma unroll
+            for (int i = 0; i < S; ++i) {
+                const int r = rg + RG * i;
+                av[i] = sm.a[s][r];
+                const float coef = sm.g[s][gidx(r)] * av[i];
+                dco[i] = 0.f;
+#pragma unroll
+                for (int q = 0; q < CPT; ++q) {
+                    const float pkc = sm.pk[s][bcol<C>(cg, q)];
+                    w[i][q] = fmaf(-coef, pkc, w[i][q]);
+                    dco[i] = fmaf(dw[i][q], pkc, dco[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < S; ++i) {
+                dco[i] += __shfl_xor_sync(0xffffffffu, dco[i], 1);
+                dco[i] += __shfl_xor_sync(0xffffffffu, dco[i], 2);
+            }
+            // 2. column sums: v1 = dW'^T coef, v2 = W^T da
+            float da[S];
+            float cv[C::NV2];
+#pragma unroll
+            for (int q = 0; q < C::NV2; ++q) cv[q] = 0.f;
+#pragma unroll
+            for (int i = 0; i < S; ++i) {
+                const int r = rg + RG * i;
+                const float g = sm.g[s][gidx(r)];
+                const float coef = g * av[i];
+                da[i] = g * dco[i];
+                if ((i & 3) == cg) sm.dgrow[r] = dco[i] * av[i];
+#pragma unroll
+                for (int q = 0; q < CPT; ++q) {
+                    cv[q] = fmaf(dw[i][q], coef, cv[q]);
+                    cv[CPT + q] = fmaf(w[i][q], da[i], cv[CPT + q]);
+                }
+            }
+            colsum(cv, 2);   // sm.vec[0] = v1, sm.vec[1] = v2 (dgrow visible too)
+            // 3. softmax backward and dbeta (warp 0) -> dz
+            if (warp == 0) {
+                float* dpk = sm.vec[0];
+                float* dpq = sm.vec[1];
+                for (int c = lane; c < D; c += 32) dpk[c] -= dpq[c];   // v1 - v2
+                __syncwarp();
+                float* pq = sm.z;   // scratch: pq = u + pk
+                for (int c = lane; c < D; c += 32) pq[c] = sm.u[s][c] + sm.pk[s][c];
+                __syncwarp();
+                warp_softmax_bwd<D>(sm.pk[s], dpk, sm.dz + D, lane);
+                warp_softmax_bwd<D>(pq, dpq, sm.dz + 2 * D, lane);
+                for (int c = lane; c < D; c += 32) sm.dz[c] = sm.dyv[s][c];
+                // dbeta per block: sum of dcoef a over the block's rows
+                float part[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int r = lane; r < M; r += 32) part[blk(r)] += sm.dgrow[r];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) part[k] = group_sum<32>(part[k]);
+                if (lane < NLR) {
+                    const float g = sm.g[s][lane];
+                    sm.dz[3 * D + lane] = part[lane] * g * (1.f - g);
+                }
+                for (int r = M + lane; r < C::MP; r += 32) sm.dz[r] = 0.f;
+            }
+            __syncthreads();
+            // 4. dW += da (outer) u + dz (outer) x~ ; column partials of W^T dz
+            float cx[C::NV1];
+#pragma unroll
+            for (int q = 0; q < C::NV1; ++q) cx[q] = 0.f;
+#pragma unroll
+            for (int i = 0; i < S; ++i) {
+                const float dzr = sm.dz[rg + RG * i];
+#pragma unroll
+                for (int q = 0; q < CPT; ++q) {
+                    const int c = bcol<C>(cg, q);
+                    dw[i][q] = fmaf(da[i], sm.u[s][c], dw[i][q]);
+                    dw[i][q] = fmaf(dzr, sm.xs[s][c], dw[i][q]);
+                    cx[q] = fmaf(w[i][q], dzr, cx[q]);
+                }
+            }
+            colsum(cx, 1);   // sm.vec[0] = dx~
+            // 5. dx (through the input softmax when present)
+            if (warp == 0) {
+                float* dxv = sm.vec[0];
+                if (softmax_input) {
+                    warp_softmax_bwd<D>(sm.xs[s], dxv, sm.vec[1], lane);
+                    __syncwarp();
+                    dxv = sm.vec[1];
+                }
+                const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
+                for (int c = lane; c < D; c += 32) bp.dx[g + c] = dxv[c];
+            }
+            __syncthreads();
+        }
+    }
+    store_tile(dw, bp.dW_seq + static_cast<size_t>(p) * MD);
+}
+
+struct BwdLaunch {
+    const void* kernel;
+    int threads;
+    int smem_bytes;
+    int kseg;
+};
+
+template <int D, int NLR>
+BwdLaunch bwd_launch_info()
+{
+    using C = BwdCfg<D, NLR>;
+    return BwdLaunch{reinterpret_cast<const void*>(&srwm_bwd_kernel<D, NLR>), C::NT,
+                     static_cast<int>(sizeof(BwdSmem<C>)), C::KSEG};
+}
+
+BwdLaunch bwd_info(int d, int n_lr);
+int launch_sum_over_batch(const float* dW_seq, float* dW0, int B, size_t per_batch, cudaStream_t stream);
+
+}  // namespace srwm

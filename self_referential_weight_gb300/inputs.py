@@ -38,7 +38,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22  # normal pairs per chunk: bounds the temporaries to ~100 MB
 
 # One tag per drawn quantity.
-TAG_X, TAG_W0, TAG_MU, TAG_LABELS = 1, 2, 3, 4
+TAG_X, TAG_W0, TAG_MU, TAG_LABELS, TAG_DY, TAG_DWF = 1, 2, 3, 4, 5, 6
 
 
 @dataclasses.dataclass(frozen=True)
@@ -148,6 +148,18 @@ def make_x(wl: Workload) -> np.ndarray:
 def make_inputs(wl: Workload):
     """(x [B,T,H,d], W0 [H,m,d]) float32 for a workload."""
     return make_x(wl), make_W0(wl.H, wl.d, wl.n_lr, wl.seed)
+
+
+def make_cotangents(wl: Workload, with_dW_final: bool = True):
+    """Output cotangents of a loss for a backward pass: (dy [B,T,H,d],
+    dW_final [B,H,m,d] or None), float32 ~ N(0, 1)."""
+    B, T, H, d = wl.B, wl.T, wl.H, wl.d
+    m = 3 * d + wl.n_lr
+    dy = normals(stream_key(wl.seed, TAG_DY), B * T * H * d).reshape(B, T, H, d)
+    dWf = None
+    if with_dW_final:
+        dWf = normals(stream_key(wl.seed, TAG_DWF), B * H * m * d).reshape(B, H, m, d)
+    return dy, dWf
 
 
 def workload(name: str, **overrides) -> Workload:

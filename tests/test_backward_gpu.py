@@ -1,0 +1,106 @@
+"""GPU parity of srwm_backward (dL/dx, dL/dW0) against the gradient oracle
+(float64 autograd through the step-by-step recurrence), on the same seeded
+inputs and cotangents.
+
+Tolerance: max|gpu - oracle| / max|oracle| <= 2e-4 per output.  The gradient
+is a sum of T backward steps in fp32, each carrying the forward's own rounding
+(<= 1e-4 relative for these lengths) into products with dL/dW; twice the
+forward's bound covers both.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import srwm_grad
+from self_referential_weight_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+TOL = 2e-4
+
+
+def rel(a, b):
+    return float(np.abs(np.asarray(a, np.float64) - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def run_bwd(x, W0, n_lr, smx, dy, dWf):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(DEV)
+    dx, dW0 = binding.srwm_backward(t(x), t(W0), n_lr, smx, t(dy), None if dWf is None else t(dWf))
+    torch.cuda.synchronize()
+    return dx.cpu().numpy(), dW0.cpu().numpy()
+
+
+def check(wl, with_dWf=True):
+    x, W0 = inputs.make_inputs(wl)
+    dy, dWf = inputs.make_cotangents(wl, with_dWf)
+    dx, dW0 = run_bwd(x, W0, wl.n_lr, wl.softmax_input, dy, dWf)
+    ox, oW = srwm_grad.grads(x, W0, wl.n_lr, wl.softmax_input, dy, dWf)
+    assert rel(dx, ox) <= TOL, rel(dx, ox)
+    assert rel(dW0, oW) <= TOL, rel(dW0, oW)
+
+
+# Segments are 32 steps: T = 75 takes two full segments and a ragged tail.
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("n_lr", [1, 4])
+@pytest.mark.parametrize("smx", [False, True])
+def test_backward_all_variants(d, n_lr, smx):
+    check(inputs.Workload("g", 2, 75, 3, d, n_lr, smx, 300 + d + n_lr + smx, "normal"))
+
+
+@pytest.mark.parametrize("d", [16, 64])
+@pytest.mark.parametrize("T", [1, 2, 31, 32, 33, 64, 65])
+def test_backward_step_count_edges(d, T):
+    check(inputs.Workload("g", 2, T, 2, d, 4, False, 400 + T, "normal"))
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_backward_without_dW_final(d):
+    check(inputs.Workload("g", 3, 40, 2, d, 4, True, 500 + d, "normal"), with_dWf=False)
+
+
+def test_backward_fewshot_episodes():
+    """The few-shot structure (one-hot label block, zero query label)."""
+    check(inputs.workload("fewshot").with_shape(B=8, H=4))
+
+
+def test_backward_longer_sequence():
+    """Several hundred steps: rounding of the stepped-back state stays within
+    one segment, so the error does not grow with T."""
+    check(inputs.Workload("g", 1, 400, 2, 64, 4, False, 600, "normal"))
+
+
+@pytest.mark.parametrize("d", [16, 64])
+def test_backward_zero_steps(d):
+    wl = inputs.Workload("g", 3, 0, 2, d, 4, False, 700, "normal")
+    W0 = inputs.make_W0(wl.H, d, 4, wl.seed)
+    _, dWf = inputs.make_cotangents(wl.with_shape(T=1))
+    x = torch.empty((3, 0, 2, d), device=DEV)
+    dx, dW0 = binding.srwm_backward(x, torch.from_numpy(W0).to(DEV), 4, False, x.clone(),
+                                    torch.from_numpy(dWf).to(DEV))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(dW0.cpu().numpy(), dWf.astype(np.float64).sum(0), rtol=1e-6, atol=1e-6)
+    dx, dW0 = binding.srwm_backward(x, torch.from_numpy(W0).to(DEV), 4, False, x.clone())
+    torch.cuda.synchronize()
+    assert not dW0.cpu().numpy().any()
+
+
+def test_backward_deterministic():
+    wl = inputs.Workload("g", 4, 70, 4, 64, 4, False, 800, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    dy, dWf = inputs.make_cotangents(wl)
+    a = run_bwd(x, W0, 4, False, dy, dWf)
+    b = run_bwd(x, W0, 4, False, dy, dWf)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_backward_small_workspace_rejected():
+    wl = inputs.Workload("g", 2, 40, 2, 16, 4, False, 900, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    dy, _ = inputs.make_cotangents(wl, False)
+    need = binding.srwm_backward_workspace_bytes(2, 40, 2, 16, 4)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    with pytest.raises(binding.SrwmError) as e:
+        binding.srwm_backward(t(x), t(W0), 4, False, t(dy), workspace=ws)
+    assert e.value.status == 2

@@ -147,3 +147,38 @@ def test_debug_segment_len_rejects_bad_values(lib):
     assert lib.srwm_debug_set_segment_len(33) == 2
     assert lib.srwm_debug_set_segment_len(-32) == 2
     assert lib.srwm_debug_set_segment_len(0) == 0
+
+
+def test_backward_workspace_bytes(lib):
+    L = lib
+    SZ, I = ctypes.c_size_t, ctypes.c_int
+    L.srwm_backward_workspace_bytes.argtypes = [I, I, I, I, I]
+    L.srwm_backward_workspace_bytes.restype = SZ
+    # 4 bytes * B * H * m * d * ceil(T / 32), rounded up to 256
+    for B, T, H, d, n_lr in [(2, 75, 3, 16, 4), (1, 32, 1, 64, 1), (5, 1, 2, 32, 4), (64, 1024, 8, 64, 4)]:
+        m = 3 * d + n_lr
+        raw = 4 * B * H * m * d * ((T + 31) // 32)
+        assert L.srwm_backward_workspace_bytes(B, T, H, d, n_lr) == (raw + 255) // 256 * 256
+    assert L.srwm_backward_workspace_bytes(2, 0, 3, 16, 4) == (4 * 2 * 3 * 52 * 16 + 255) // 256 * 256
+    assert L.srwm_backward_workspace_bytes(2, 5, 3, 48, 4) == 0
+    assert L.srwm_backward_workspace_bytes(2, 5, 3, 16, 2) == 0
+    assert L.srwm_backward_workspace_bytes(0, 5, 3, 16, 4) == 0
+
+
+def test_backward_validation(lib):
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.srwm_backward.argtypes = [P, P, I, I, I, I, I, I, P, P, P, P, P, SZ, P]
+    big = 1 << 40
+
+    def bwd(x=A, W0=A + 0x1000000, B=2, T=3, H=2, d=16, n_lr=4, smx=0, dy=A + 0x2000000, dWf=None,
+            dx=A + 0x3000000, dW0=A + 0x4000000, ws=A + 0x5000000, ws_bytes=big):
+        return lib.srwm_backward(x, W0, B, T, H, d, n_lr, smx, dy, dWf, dx, dW0, ws, ws_bytes, None)
+
+    assert bwd(x=None) == 1 and bwd(dy=None) == 1 and bwd(dx=None) == 1
+    assert bwd(W0=None) == 1 and bwd(dW0=None) == 1 and bwd(ws=None) == 1
+    assert bwd(B=0) == 2 and bwd(T=-1) == 2
+    assert bwd(d=8) == 3 and bwd(n_lr=2) == 3 and bwd(smx=2) == 3
+    assert bwd(ws_bytes=1024) == 2          # too small for these sizes
+    assert bwd(dx=A + 0x3000004) == 4       # misaligned
+    assert bwd(dx=A + 0x2000000) == 5       # dx on top of dy
+    assert bwd(ws=A) == 5                   # workspace over x
