@@ -36,8 +36,13 @@ METRIC = "SRWM head-token updates/s (B*T*H/s) and % of FP32 FMA peak, 1 GB300"
 UNIT = "head-token updates/s"
 FMA_PER_CLK_PER_SM = 128          # FP32 FMA lanes per SM (4 SMSPs x 32)
 L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "srwm_d64_kernel_mid.md")
-KERNEL_SOURCES = ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"]
+# Source files of each kernel; a committed ncu summary is used only while
+# their hash matches the one recorded in it.
+KERNEL_SOURCES = {
+    "srwm_d64_kernel": ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
+    "srwm_d64w2_kernel": ["srwm_d64w2.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
+    "srwm_warp_kernel": ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h"],
+}
 
 
 def parse():
@@ -82,25 +87,36 @@ def fmas_per_head_token(wl):
     return 3 * wl.m * wl.d
 
 
-def kernel_source_hash():
+def kernel_name(wl, n_sm):
+    """The kernel the library launches for this workload (see srwm_d64.cu)."""
+    if wl.d != 64:
+        return "srwm_warp_kernel"
+    return "srwm_d64w2_kernel" if wl.B * wl.H > 2 * n_sm else "srwm_d64_kernel"
+
+
+def profile_summary_path(kernel, workload):
+    return os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "self_referential_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     this workload with the current kernel sources; else None."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(profile_summary_path(kernel, workload)).read()
     except OSError:
         return None
     src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     wl = re.search(r"workload:\s*(\w+)", text)
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not (src and wl and tr) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
+    if not (src and wl and tr) or src.group(1) != kernel_source_hash(kernel) or wl.group(1) != workload:
         return None
     return int(tr.group(1))
 
@@ -383,8 +399,8 @@ def main():
             "peak": peak_tflops,
             "unit": "TFLOP/s",
             "frac": achieved / peak_tflops,
-            "traffic": profiled_traffic(wl.name),
-            "kernel": "srwm_d64_kernel" if wl.d == 64 else "srwm_warp_kernel",
+            "traffic": profiled_traffic(kernel_name(wl, n_sm), wl.name),
+            "kernel": kernel_name(wl, n_sm),
             "flops_per_launch": flops_per_launch,
             "peak_basis": f"{n_sm} SMs x {FMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 flop x "
                           f"{f_max_mhz:.0f} MHz (max SM clock)",

@@ -110,11 +110,25 @@ int make_stream_map(CUtensorMap* map, const float* base, int B, int T, int H, in
     return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
 }
 
-srwm::LaunchInfo info_for(int d, int n_lr, int smx)
+// The kernel for a call; at d = 64 it depends on the streams per SM.
+int info_for(int d, int n_lr, int smx, long long n_streams, srwm::LaunchInfo* li)
 {
-    if (d == 16) return srwm::launch_info_d16(n_lr, smx);
-    if (d == 32) return srwm::launch_info_d32(n_lr, smx);
-    return srwm::launch_info_d64(n_lr, smx);
+    if (d == 16) {
+        *li = srwm::launch_info_d16(n_lr, smx);
+        return SRWM_OK;
+    }
+    if (d == 32) {
+        *li = srwm::launch_info_d32(n_lr, smx);
+        return SRWM_OK;
+    }
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    *li = srwm::launch_info_d64(n_lr, smx, n_streams, n_sm);
+    return SRWM_OK;
 }
 
 int check_params(int B, int T, int H, int d, int n_lr, int softmax_input)
@@ -229,7 +243,8 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
         if ((rc = check_device_ptr(y)) != SRWM_OK) return rc;
     }
 
-    const srwm::LaunchInfo li = info_for(d, n_lr, smx);
+    srwm::LaunchInfo li;
+    if ((rc = info_for(d, n_lr, smx, static_cast<long long>(B) * H, &li)) != SRWM_OK) return rc;
     CUtensorMap tx, ty;
     std::memset(&tx, 0, sizeof(tx));
     std::memset(&ty, 0, sizeof(ty));

@@ -48,6 +48,6 @@ struct LaunchInfo {
 
 LaunchInfo launch_info_d16(int n_lr, int softmax_input);
 LaunchInfo launch_info_d32(int n_lr, int softmax_input);
-LaunchInfo launch_info_d64(int n_lr, int softmax_input);
+LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm);
 
 }  // namespace srwm

@@ -1,14 +1,24 @@
-// srwm_d64.cu -- instantiations of the d = 64 kernel (one translation unit
+// srwm_d64.cu -- instantiations of the d = 64 kernels (one translation unit
 // per width so the library builds in parallel).
 #include "srwm_d64.cuh"
+#include "srwm_d64w2.cuh"
 
 namespace srwm {
 
-// Four warps per stream.  (Eight warps per stream, one stream per SM, was
-// measured slower on the long workload: each warp reloads the step's vectors
-// from shared memory, and that traffic grows with the warp count.)
-LaunchInfo launch_info_d64(int n_lr, int softmax_input)
+// Two kernels, chosen by the number of (sequence, head) streams per SM:
+//   * up to two per SM: four warps per stream (two CTAs per SM).  Each stream
+//     then has a slot of its own, and four warps give the shortest step.
+//     (Eight warps per stream, one stream per SM, was measured slower on the
+//     long workload: each warp reloads the step's vectors from shared memory,
+//     and that traffic grows with the warp count.)
+//   * more: two warps per stream, four CTAs per SM, so twice as many streams
+//     advance at once.
+LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm)
 {
+    if (n_streams > 2LL * n_sm) {
+        if (n_lr == 1) return softmax_input ? launch_info_d64w2_impl<1, true>() : launch_info_d64w2_impl<1, false>();
+        return softmax_input ? launch_info_d64w2_impl<4, true>() : launch_info_d64w2_impl<4, false>();
+    }
     if (n_lr == 1) return softmax_input ? launch_info_d64_impl<4, 1, true>() : launch_info_d64_impl<4, 1, false>();
     return softmax_input ? launch_info_d64_impl<4, 4, true>() : launch_info_d64_impl<4, 4, false>();
 }

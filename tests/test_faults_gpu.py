@@ -24,21 +24,25 @@ def short_waits():
     binding.srwm_set_wait_limit_ns(1_000_000_000)
 
 
-@pytest.mark.parametrize("d", [16, 32, 64])
-def test_missing_chunk_times_out_then_recovers(short_waits, d):
-    wl = inputs.Workload("t", 2, 100, 3, d, 4, False, 40 + d, "normal")
+@pytest.mark.parametrize("d,B,smx", [(16, 2, False), (32, 2, False), (64, 2, False), (64, 110, False),
+                                     (64, 110, True)])
+def test_missing_chunk_times_out_then_recovers(short_waits, d, B, smx):
+    """B = 110 (330 streams at H = 3, more than two per SM on a GB300) runs the
+    two-warp d = 64 kernel, whose CTAs agree on a timeout at chunk boundaries,
+    with and without the input softmax."""
+    wl = inputs.Workload("t", B, 100, 3, d, 4, smx, 40 + d, "normal")
     x, W0 = inputs.make_inputs(wl)
     xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
     assert binding.srwm_last_device_status() == 0
 
     binding.srwm_debug_skip_x_chunk(1)
-    binding.srwm_forward(xd, W0d, 4)
+    binding.srwm_forward(xd, W0d, 4, smx)
     assert binding.srwm_last_device_status() == binding.SRWM_ERR_TIMEOUT
     assert binding.srwm_last_device_status() == 0  # reading clears it
 
     binding.srwm_debug_skip_x_chunk(-1)
-    y, Wf = binding.srwm_forward(xd, W0d, 4)
+    y, Wf = binding.srwm_forward(xd, W0d, 4, smx)
     assert binding.srwm_last_device_status() == 0
-    yo, Wo = oracle.forward(x, W0, 4)
+    yo, Wo = oracle.forward(x, W0, 4, smx)
     assert np.abs(y.cpu().numpy() - yo).max() / np.abs(yo).max() <= 1e-4
     assert np.abs(Wf.cpu().numpy() - Wo).max() / np.abs(Wo).max() <= 1e-4

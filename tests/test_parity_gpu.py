@@ -218,6 +218,70 @@ def test_d64_more_streams_than_sms(n_lr, smx):
     assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
 
 
+def many_stream_batch(n_sm):
+    """B for H = 8 streams per sequence so that d = 64 runs more than two
+    streams per SM (the two-warp kernel), with a partly filled last wave."""
+    return (2 * n_sm) // 8 + 3
+
+
+@pytest.mark.parametrize("n_lr", [1, 4])
+@pytest.mark.parametrize("smx", [False, True])
+def test_d64_many_streams_all_variants(n_lr, smx):
+    """More than two d = 64 streams per SM selects two warps per stream (four
+    CTAs per SM); checked in full against the oracle over several TMA chunks
+    and a ragged tail."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = inputs.Workload("t", many_stream_batch(n_sm), 75, 8, 64, n_lr, smx, 130 + n_lr + smx, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 64])
+def test_d64_many_streams_step_edges(T):
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = inputs.Workload("t", many_stream_batch(n_sm), T, 8, 64, 4, False, 140 + T, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, 4, False)
+    yo, Wo = oracle.forward(x, W0, 4, False)
+    assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
+
+
+def test_d64_many_streams_slice_and_determinism():
+    """A stream computed alone (four-warp kernel) equals the same stream in a
+    many-stream batch (two-warp kernel) within fp32 rounding; the batch is
+    bitwise repeatable."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = inputs.Workload("t", many_stream_batch(n_sm), 70, 8, 64, 4, False, 150, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, 4, False)
+    y2, Wf2 = run_gpu(x, W0, 4, False)
+    np.testing.assert_array_equal(y, y2)
+    np.testing.assert_array_equal(Wf, Wf2)
+    b, h = wl.B - 2, 5
+    ys, Ws = run_gpu(np.ascontiguousarray(x[b:b + 1, :, h:h + 1]), np.ascontiguousarray(W0[h:h + 1]), 4, False)
+    assert rel(y[b, :, h], ys[0, :, 0]) <= 1e-5 and rel(Wf[b, h], Ws[0, 0]) <= 1e-5
+
+
+def test_d64_many_streams_step_chains_to_forward():
+    """srwm_step over many per-sequence states (two-warp kernel, T = 1),
+    chained in place, equals srwm_forward."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = inputs.Workload("t", many_stream_batch(n_sm), 9, 8, 64, 4, True, 160, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, 4, True)
+    xd = torch.from_numpy(x).to(DEV)
+    W = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(W0, (wl.B,) + W0.shape))).to(DEV)
+    ys = []
+    for t in range(wl.T):
+        yt, W = binding.srwm_step(xd[:, t].contiguous(), W, 4, True, W_out=W)
+        ys.append(yt.cpu().numpy())
+    torch.cuda.synchronize()
+    assert binding.srwm_last_device_status() == 0
+    assert rel(np.stack(ys, axis=1), y) <= 1e-5 and rel(W.cpu().numpy(), Wf) <= 1e-5
+
+
 @pytest.mark.parametrize("d", [16, 32, 64])
 @pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
 def test_forward_from_resumes_a_split_sequence(d, n_lr, smx):
@@ -272,6 +336,28 @@ def test_balanced_forced_segments_match(d, n_lr, smx):
     assert rel(yb, y) <= 1e-5 and rel(Wb, Wf) <= 1e-5
     np.testing.assert_array_equal(yb, yb2.cpu().numpy())
     np.testing.assert_array_equal(Wb, Wb2.cpu().numpy())
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    assert rel(yb, yo) <= 1e-4 and rel(Wb, Wo) <= 1e-4
+
+
+@pytest.mark.parametrize("n_lr,smx", [(4, False), (1, True)])
+def test_balanced_forced_segments_many_streams(n_lr, smx):
+    """The balanced schedule on the two-warp d = 64 kernel: more streams than
+    its slots' worth per wave, forced 32-step segments."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = inputs.Workload("t", (5 * n_sm) // 8 + 1, 100, 8, 64, n_lr, smx, 170 + n_lr, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
+    binding.srwm_debug_set_segment_len(32)
+    try:
+        yb, Wb = binding.srwm_forward_balanced(xd, W0d, n_lr, smx)
+        torch.cuda.synchronize()
+        assert binding.srwm_last_device_status() == 0
+    finally:
+        binding.srwm_debug_set_segment_len(0)
+    yb, Wb = yb.cpu().numpy(), Wb.cpu().numpy()
+    assert rel(yb, y) <= 1e-5 and rel(Wb, Wf) <= 1e-5
     yo, Wo = oracle.forward(x, W0, n_lr, smx)
     assert rel(yb, yo) <= 1e-4 and rel(Wb, Wo) <= 1e-4
 
