@@ -33,6 +33,9 @@
 // z is double-buffered by step parity (a fast warp writes z_{t+1} while a slow
 // one still reads z_t); y staging is triple-buffered (one chunk being written,
 // up to two still read by bulk stores).
+// Without the input softmax x~ = x is read straight from the TMA ring, and the
+// steps run chunk by chunk, with the chunk-boundary work between chunks
+// rather than in every step (measured: 6.44 -> 5.34 ms on the long workload).
 #pragma once
 
 #include <cuda.h>
@@ -95,7 +98,8 @@ __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&o
 template <int NW, int NS, int NLR>
 __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int lane, int warp, int rg, int cg,
                                          float2 (&w)[d64::Cfg<NW>::SLOTS + 1][d64::NP],
-                                         float (&coef)[d64::Cfg<NW>::SLOTS + 1], float2 (&pkc)[d64::NP])
+                                         float (&coef)[d64::Cfg<NW>::SLOTS + 1], float2 (&pkc)[d64::NP],
+                                         const float* xn)
 {
     using namespace d64;
     using C = Cfg<NW>;
@@ -110,7 +114,7 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
     const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
 
     float2 x2[NP];
-    load_pairs(sm.xs[(t + 1) & 1], cg, x2);
+    load_pairs(xn, cg, x2);
     float2 accb[NS];
 #pragma unroll
     for (int i = 0; i < NS; ++i) accb[i] = make_float2(0.f, 0.f);
@@ -299,8 +303,10 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
             if (nchunks > 1) issue_chunk(1);
             if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], parity(0) & 1, kp.wait_limit_ns))) {
                 landed = 0;
-                stage_x(0, sm.xs[0]);
-                stage_x(1, sm.xs[1]);
+                if constexpr (SMX) {
+                    stage_x(0, sm.xs[0]);
+                    stage_x(1, sm.xs[1]);
+                }
             } else {
                 fail = 1;
             }
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
         // ---- prologue: z_0 = W x~_0 (y of the item's first step)
         if (!abort && T > 0) {
             float2 x2[NP];
-            load_pairs(sm.xs[0], cg, x2);
+            load_pairs(SMX ? sm.xs[0] : sm.xring[0][0], cg, x2);
             float2 acc[S1];
 #pragma unroll
             for (int i = 0; i < S1; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -349,36 +355,79 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
 #pragma unroll
         for (int q = 0; q < NP; ++q) pkc[q] = make_float2(0.f, 0.f);
 
-        for (int t = 0; t < T && !abort; ++t) {
-            // y chunk holding y_t complete -> TMA store
-            if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
-                const int c = t / TAU;
-                tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
-                bulk_commit();
-                bulk_wait_read<1>();
-            }
-            // Warp 0 also carries the beta rows; a compile-time slot count keeps
-            // each role's step free of branches.
-            if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
-            else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc);
-
-            // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
-            fail = 0;
-            if (warp == XW) {
-                const int tn = t + 2;
-                if (tn < T && tn % TAU == 0) {
-                    const int c = tn / TAU;
+        // Warp 0 also carries the beta rows; a compile-time slot count keeps
+        // each role's step free of branches.
+        auto step = [&](int t, const float* xn) {
+            if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn);
+            else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn);
+        };
+        if constexpr (!SMX) {
+            // x~ = x is read straight from the ring, chunk by chunk: the inner
+            // loop holds only the step and its barrier; the chunk boundary
+            // (bounded wait for the next chunk, agreed on by the CTA, the next
+            // TMA load, the y store) runs between chunks.
+            for (int c0 = 0; c0 < T && !abort; c0 += TAU) {
+                const int tend = min(c0 + TAU, T);
+                const float* ring = sm.xring[(c0 / TAU) & 1][0];
+                for (int t = c0; t < tend - 1; ++t) {
+                    step(t, ring + (t + 1 - c0) * D);
+                    __syncthreads();
+                }
+                const float* xn = ring;   // unused past the end of the item
+                if (tend < T) {
+                    // chunk c is read from the next step on; its buffer's previous
+                    // chunk c-2 was last read two chunks ago, and chunk c+1 goes into
+                    // the current buffer, whose last read was the step before this one
+                    const int c = tend / TAU;
                     const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c) & 1, kp.wait_limit_ns);
-                    if (__all_sync(0xffffffffu, ok)) {
+                    if (__syncthreads_or(!ok)) {
+                        abort = 1;
+                        break;
+                    }
+                    if (warp == XW) {
                         landed = c;
                         if (c + 1 < nchunks) issue_chunk(c + 1);
-                    } else {
-                        fail = 1;
                     }
+                    xn = sm.xring[c & 1][0];
                 }
-                if (!fail) stage_x(tn, sm.xs[t & 1]);
+                step(tend - 1, xn);
+                __syncthreads();
+                // y of the chunk's steps complete -> TMA store
+                if (warp == 0 && lane == 0 && tend % TAU == 0) {
+                    tma_store_4d(&tmy, &sm.ystage[(c0 / TAU) % 3][0][0], 0, h, t0 + c0, b);
+                    bulk_commit();
+                    bulk_wait_read<1>();
+                }
             }
-            abort = __syncthreads_or(fail);
+        } else {
+            for (int t = 0; t < T && !abort; ++t) {
+                // y chunk holding y_t complete -> TMA store
+                if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
+                    const int c = t / TAU;
+                    tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
+                    bulk_commit();
+                    bulk_wait_read<1>();
+                }
+                step(t, sm.xs[(t + 1) & 1]);
+
+                // ---- x~_{t+2} -> xs[t & 1] (a new chunk may have to land first)
+                fail = 0;
+                if (warp == XW) {
+                    const int tn = t + 2;
+                    if (tn < T && tn % TAU == 0) {
+                        const int c = tn / TAU;
+                        const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c) & 1, kp.wait_limit_ns);
+                        if (__all_sync(0xffffffffu, ok)) {
+                            landed = c;
+                            if (c + 1 < nchunks) issue_chunk(c + 1);
+                        } else {
+                            fail = 1;
+                        }
+                    }
+                    if (!fail) stage_x(tn, sm.xs[t & 1]);
+                }
+                abort = __syncthreads_or(fail);
+            }
         }
 
         // ---- drain this item's y stores
