@@ -25,9 +25,9 @@
 // W and little else stays resident in the 255 registers.
 //
 // One step:
-//   1. the pending rank-one update of the previous step (scalar FMAs, which
-//      need no duplicated coefficient pairs); meanwhile phi_k, phi_q of z_t in
-//      the lane layout (entries lane, lane + 32);
+//   1. the pending rank-one update of the previous step (two-wide FMAs with
+//      the coefficient duplicated into a pair); meanwhile phi_k, phi_q of z_t
+//      in the lane layout (entries lane, lane + 32);
 //   2. phi_k and u = phi_q - phi_k go to the warp's own buffer (by step
 //      parity); s = phi_k . x~_{t+1} as a warp sum;
 //   3. a-dots against u and b-dots against x~_{t+1}, reductions, gates;
@@ -115,10 +115,9 @@ __device__ __forceinline__ void d64w2_step(d64w2::Smem& sm, int t, int T, int la
         const float4 p4 = ld4s(pk_prev + 4 * (cg + 2 * j));
 #pragma unroll
         for (int i = 0; i < SL; ++i) {
-            w[i][2 * j].x = fmaf(coef[i], p4.x, w[i][2 * j].x);
-            w[i][2 * j].y = fmaf(coef[i], p4.y, w[i][2 * j].y);
-            w[i][2 * j + 1].x = fmaf(coef[i], p4.z, w[i][2 * j + 1].x);
-            w[i][2 * j + 1].y = fmaf(coef[i], p4.w, w[i][2 * j + 1].y);
+            const float2 cc = make_float2(coef[i], coef[i]);
+            w[i][2 * j] = __ffma2_rn(cc, lo2(p4), w[i][2 * j]);
+            w[i][2 * j + 1] = __ffma2_rn(cc, hi2(p4), w[i][2 * j + 1]);
         }
     }
     {
