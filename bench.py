@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--layer", action="store_true",
+                    help="time one Recursive Self-Transformer layer (SRWM + LN + FF + residual, d_ff = 4D) "
+                         "on the workload's shape instead; prints its own line")
     return ap.parse_args()
 
 
@@ -253,6 +256,8 @@ def main():
     rank, world, local = dist_env()
     wl = inputs.workload(args.workload)
 
+    if args.layer:
+        return bench_layer(args, wl)
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, wl)
@@ -453,6 +458,76 @@ def fma_probe(binding, n_sm, stream):
         fmas = blocks * threads * iters * 8 * (2 if packed else 1)
         res["tflops_packed" if packed else "tflops_scalar"] = 2 * fmas / s / 1e12
     return res
+
+
+def bench_layer(args, wl):
+    """One Recursive Self-Transformer layer on the workload's shape: tokens/s
+    of srwm_layer_forward, its SRWM part alone, and the feed-forward GEMMs with
+    emulated and plain FP32 (1 GPU, L2 flushed between timed calls)."""
+    import torch
+    from self_referential_weight_gb300 import binding
+
+    dev = torch.device("cuda:0")
+    D, d_ff = wl.H * wl.d, 4 * wl.H * wl.d
+    p = {k: torch.from_numpy(v).to(dev) for k, v in inputs.make_layer_params(wl.H, wl.d, wl.n_lr, d_ff, wl.seed).items()}
+    u = torch.from_numpy(inputs.make_layer_input(wl.B, wl.T, D, wl.seed)).to(dev)
+    out = torch.empty_like(u)
+    ws = torch.empty(binding.srwm_layer_workspace_bytes(wl.B, wl.T, wl.H, wl.d, wl.n_lr, d_ff), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def layer():
+        binding.srwm_layer_forward(u, wl.H, wl.n_lr, wl.softmax_input, p["ln1_gamma"], p["ln1_beta"], p["W0"],
+                                   p["ln2_gamma"], p["ln2_beta"], p["W1"], p["b1"], p["W2"], p["b2"], out=out,
+                                   workspace=ws)
+
+    x4 = u.view(wl.B, wl.T, wl.H, wl.d)
+    y = torch.empty_like(x4)
+    Wf = torch.empty((wl.B, wl.H, wl.m, wl.d), device=dev)
+    cnt = torch.empty(binding.srwm_forward_workspace_bytes(wl.B, wl.H), dtype=torch.uint8, device=dev)
+
+    def srwm():
+        binding.srwm_forward_balanced(x4, p["W0"], wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, workspace=cnt)
+
+    def timed(fn, steps):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        if binding.srwm_last_device_status() != 0:
+            raise RuntimeError("device status set")
+        return statistics.median(ts)
+
+    steps = max(3, min(args.steps, 20))
+    t_layer = timed(layer, steps)
+    t_srwm = timed(srwm, steps)
+    binding.srwm_debug_set_layer_gemm(True)
+    try:
+        t_plain = timed(layer, steps)
+    finally:
+        binding.srwm_debug_set_layer_gemm(False)
+    tokens = wl.B * wl.T
+    ff_flops = 2 * 2 * tokens * D * d_ff
+    print(json.dumps({
+        "metric": "Recursive Self-Transformer layer forward, tokens/s (1 GB300)",
+        "value": tokens / (t_layer / 1e3), "unit": "tokens/s", "ms_per_step": t_layer, "steps": steps,
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d": wl.d, "D": D, "d_ff": d_ff,
+                   "n_lr": wl.n_lr, "softmax_input": wl.softmax_input, "l2": "flushed between timed steps"},
+        "dtype": "f32", "data": "synthetic",
+        "parts_ms": {"srwm_forward_alone": t_srwm, "layer_minus_srwm": t_layer - t_srwm},
+        "ff_gemm_flops": ff_flops,
+        "ff_plus_ln_tflops_emulated_fp32": ff_flops / ((t_layer - t_srwm) / 1e3) / 1e12,
+        "ms_per_step_plain_fp32_gemm": t_plain,
+        "ff_plus_ln_tflops_plain_fp32": ff_flops / ((t_plain - t_srwm) / 1e3) / 1e12,
+    }), flush=True)
 
 
 if __name__ == "__main__":

@@ -191,6 +191,52 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
  */
 size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr);
 
+/*
+ * srwm_layer_forward -- one Recursive Self-Transformer layer, forward: the
+ * multi-head SRWM in place of multi-head self-attention, with the
+ * Transformer's layer norms, feed-forward block and residual connections
+ * around it ("Metalearning Continual Learning Algorithms", section 2.3; the
+ * review "SRWM:让权重矩阵学习修改自身", section 2.4).  Pre-LN block over the
+ * N = B*T tokens of width D = H*d:
+ *   a = LN1(u);  y = SRWM(a) (as srwm_forward, heads = d-wide slices);
+ *   h = u + y;   out = h + W2 ReLU(W1 LN2(h) + b1) + b2
+ * LN(v) = (v - mean(v)) / sqrt(var(v) + 1e-5) * gamma + beta over the D
+ * entries of a token (biased variance).  Everything is fp32; the two
+ * feed-forward products are cuBLASLt GEMMs with fp32 inputs and outputs
+ * (FP32 emulated on the BF16 tensor cores where offered, see
+ * srwm_debug_set_layer_gemm), the rest runs in this library's kernels.
+ *
+ *   u          [B, T, D]      input tokens
+ *   ln*_gamma, ln*_beta [D]   layer-norm scale and shift
+ *   W0         [H, m, d]      SRWM initial state (as srwm_forward)
+ *   W1 [d_ff, D], b1 [d_ff], W2 [D, d_ff], b2 [D]   feed-forward (row-major,
+ *              output index first, as a PyTorch Linear weight)
+ *   out        [B, T, D]      written
+ *   W_final    [B, H, m, d]   the SRWM's final state, written; or NULL
+ *   workspace  device scratch of srwm_layer_workspace_bytes(...) bytes,
+ *              16-byte aligned, untouched until the work on `stream` ends
+ *
+ * Supported: D = H*d <= 1024, d_ff a positive multiple of 4, and the
+ * srwm_forward limits.  The same pointer rules apply: outputs and workspace
+ * overlap nothing else.
+ */
+int srwm_layer_forward(const float* u, int B, int T, int H, int d, int n_lr, int softmax_input,
+                       const float* ln1_gamma, const float* ln1_beta, const float* W0,
+                       const float* ln2_gamma, const float* ln2_beta, const float* W1,
+                       const float* b1, int d_ff, const float* W2, const float* b2, float* out,
+                       float* W_final, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes srwm_layer_forward needs for these sizes; 0 when unsupported. */
+size_t srwm_layer_workspace_bytes(int B, int T, int H, int d, int n_lr, int d_ff);
+
+/*
+ * srwm_debug_set_layer_gemm -- how srwm_layer_forward's feed-forward GEMMs
+ * compute: 0 (default) FP32 emulated on the BF16 tensor cores where cuBLASLt
+ * offers it (fp32-level accuracy), else plain FP32; 1 plain FP32 only.  For
+ * comparisons; applies to calls made afterwards.
+ */
+int srwm_debug_set_layer_gemm(int plain_fp32);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* srwm_status_string(int status);
 

@@ -20,7 +20,8 @@ SRWM_ERR_TIMEOUT = 7
 
 EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noalloc",
            "srwm_forward_workspace_bytes", "srwm_forward_from",
-           "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
+           "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes",
+           "srwm_layer_forward", "srwm_layer_workspace_bytes", "srwm_debug_set_layer_gemm", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
            "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
 
 
@@ -64,6 +65,12 @@ def _lib():
         lib.srwm_backward.restype = I
         lib.srwm_backward_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.srwm_backward_workspace_bytes.restype = SZ
+        lib.srwm_layer_forward.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P, SZ, P]
+        lib.srwm_layer_forward.restype = I
+        lib.srwm_layer_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.srwm_layer_workspace_bytes.restype = SZ
+        lib.srwm_debug_set_layer_gemm.argtypes = [I]
+        lib.srwm_debug_set_layer_gemm.restype = I
         lib.srwm_status_string.argtypes = [I]
         lib.srwm_status_string.restype = ctypes.c_char_p
         lib.srwm_last_device_status.argtypes = [P]
@@ -238,6 +245,42 @@ def srwm_backward(x, W0, n_lr, softmax_input, dy, dW_final=None, dx=None, dW0=No
                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc, "srwm_backward")
     return dx, dW0
+
+
+def srwm_layer_workspace_bytes(B, T, H, d, n_lr, d_ff) -> int:
+    return int(_lib().srwm_layer_workspace_bytes(int(B), int(T), int(H), int(d), int(n_lr), int(d_ff)))
+
+
+def srwm_layer_forward(u, H, n_lr, softmax_input, ln1_gamma, ln1_beta, W0, ln2_gamma, ln2_beta, W1, b1, W2, b2,
+                       out=None, W_final=None, workspace=None, stream=None):
+    """One Recursive Self-Transformer layer: u [B,T,D] -> out [B,T,D] (D = H*d).
+
+    Parameters as in include/srwm.h (W1 [d_ff,D], W2 [D,d_ff], PyTorch Linear
+    layout).  W_final [B,H,m,d] receives the SRWM's final state when given."""
+    B, T, D = u.shape
+    d = D // H
+    m = 3 * d + n_lr
+    d_ff = W1.shape[0]
+    if out is None:
+        out = torch.empty((B, T, D), dtype=torch.float32, device=u.device)
+    need = srwm_layer_workspace_bytes(B, T, H, d, n_lr, d_ff)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=u.device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    pwf = _dev(W_final, "W_final", (B, H, m, d)) if W_final is not None else ctypes.c_void_p(0)
+    rc = _lib().srwm_layer_forward(
+        _dev(u, "u"), B, T, H, d, int(n_lr), int(bool(softmax_input)), _dev(ln1_gamma, "ln1_gamma", (D,)),
+        _dev(ln1_beta, "ln1_beta", (D,)), _dev(W0, "W0", (H, m, d)), _dev(ln2_gamma, "ln2_gamma", (D,)),
+        _dev(ln2_beta, "ln2_beta", (D,)), _dev(W1, "W1", (d_ff, D)), _dev(b1, "b1", (d_ff,)), d_ff,
+        _dev(W2, "W2", (D, d_ff)), _dev(b2, "b2", (D,)), _dev(out, "out", (B, T, D)), pwf,
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "srwm_layer_forward")
+    return out, W_final
+
+
+def srwm_debug_set_layer_gemm(plain_fp32: bool) -> None:
+    _check(_lib().srwm_debug_set_layer_gemm(int(bool(plain_fp32))), "srwm_debug_set_layer_gemm")
 
 
 def srwm_last_device_status(stream=None) -> int:

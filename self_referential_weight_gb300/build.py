@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsrwm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["srwm_api.cu", "srwm_d16.cu", "srwm_d32.cu", "srwm_d64.cu", "srwm_probe.cu", "srwm_noalloc.cu", "srwm_bwd.cu"]
+UNITS = ["srwm_api.cu", "srwm_d16.cu", "srwm_d32.cu", "srwm_d64.cu", "srwm_probe.cu", "srwm_noalloc.cu", "srwm_bwd.cu",
+         "srwm_layer.cu"]
 
 
 def _nvcc() -> str:
@@ -66,7 +67,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
         objs = list(ex.map(compile_unit, UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
+    # cuBLASLt (the layer's two feed-forward GEMMs) from the toolkit next to nvcc
+    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-L", libdir, "-lcublasLt",
+           "-Xlinker", f"-rpath,{libdir}"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"linking libsrwm.so failed:\n{res.stdout}\n{res.stderr}")

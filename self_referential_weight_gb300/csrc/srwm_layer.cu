@@ -1,0 +1,332 @@
+// srwm_layer.cu -- one Recursive Self-Transformer layer, forward: the SRWM in
+// place of multi-head self-attention, with the Transformer's layer norms,
+// feed-forward block and residual connections around it
+// ("Metalearning Continual Learning Algorithms", section 2.3; the review
+// "SRWM:让权重矩阵学习修改自身", section 2.4, keeps those blocks unchanged).
+//
+// Pre-LN block, N = B*T tokens of width D = H*d:
+//   a   = LN1(u)                       (this file: ln_kernel)
+//   y   = SRWM(a)                      (the recurrence kernels; heads = d-wide slices of a)
+//   h   = u + y;  b = LN2(h)           (ln_kernel with the residual add fused)
+//   f   = ReLU(b W1^T + b1)            (cuBLASLt, fp32, bias + ReLU epilogue)
+//   out = h + f W2^T + b2              (cuBLASLt, fp32, bias epilogue, accumulating onto h)
+// The two feed-forward products are plain dense GEMMs and go to the library;
+// everything else runs in this library's kernels.
+#include <cublasLt.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <utility>
+
+#include "srwm.h"
+
+namespace {
+
+constexpr float kLnEps = 1e-5f;
+constexpr int kLnMaxQuads = 8;                     // float4 per lane: D <= 32 * 4 * 8 = 1024
+constexpr size_t kLtWorkspace = 32u << 20;         // cuBLASLt scratch inside the caller's workspace
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// One warp per row of D floats (D % 4 == 0, D <= 1024): v = a (+ r);
+// optionally h_out = v; out = (v - mean) / sqrt(var + eps) * g + beta, with
+// the mean and the variance (of deviations from the mean) as fixed-order warp
+// sums, so the result is deterministic.
+template <bool RESIDUAL>
+__global__ void __launch_bounds__(256) ln_kernel(const float* __restrict__ a, const float* __restrict__ r,
+                                                 float* __restrict__ h_out, const float* __restrict__ g,
+                                                 const float* __restrict__ beta, float* __restrict__ out,
+                                                 long long rows, int D)
+{
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;   // warp-uniform
+    const int quads = D >> 2;
+    const float4* av = reinterpret_cast<const float4*>(a + row * D);
+    float4 v[kLnMaxQuads];
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnMaxQuads; ++k) {
+        const int q = lane + 32 * k;
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q < quads) {
+            v[k] = av[q];
+            if constexpr (RESIDUAL) {
+                const float4 rr = reinterpret_cast<const float4*>(r + row * D)[q];
+                v[k].x += rr.x;
+                v[k].y += rr.y;
+                v[k].z += rr.z;
+                v[k].w += rr.w;
+                reinterpret_cast<float4*>(h_out + row * D)[q] = v[k];
+            }
+            sum += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mean = sum / static_cast<float>(D);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnMaxQuads; ++k) {
+        const int q = lane + 32 * k;
+        if (q < quads) {
+            const float dx = v[k].x - mean, dy = v[k].y - mean, dz = v[k].z - mean, dw = v[k].w - mean;
+            ss += (dx * dx + dy * dy) + (dz * dz + dw * dw);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rstd = 1.0f / sqrtf(ss / static_cast<float>(D) + kLnEps);
+#pragma unroll
+    for (int k = 0; k < kLnMaxQuads; ++k) {
+        const int q = lane + 32 * k;
+        if (q < quads) {
+            const float4 gg = reinterpret_cast<const float4*>(g)[q];
+            const float4 bb = reinterpret_cast<const float4*>(beta)[q];
+            float4 o4;
+            o4.x = (v[k].x - mean) * rstd * gg.x + bb.x;
+            o4.y = (v[k].y - mean) * rstd * gg.y + bb.y;
+            o4.z = (v[k].z - mean) * rstd * gg.z + bb.z;
+            o4.w = (v[k].w - mean) * rstd * gg.w + bb.w;
+            reinterpret_cast<float4*>(out + row * D)[q] = o4;
+        }
+    }
+}
+
+int launch_ln(bool residual, const float* a, const float* r, float* h_out, const float* g, const float* beta,
+              float* out, long long rows, int D, cudaStream_t st)
+{
+    if (rows == 0) return SRWM_OK;
+    const int warps = 8;
+    const long long blocks = (rows + warps - 1) / warps;
+    if (blocks > 0x7fffffffLL) return SRWM_ERR_SHAPE;
+    if (residual)
+        ln_kernel<true><<<static_cast<unsigned>(blocks), 32 * warps, 0, st>>>(a, r, h_out, g, beta, out, rows, D);
+    else
+        ln_kernel<false><<<static_cast<unsigned>(blocks), 32 * warps, 0, st>>>(a, r, h_out, g, beta, out, rows, D);
+    return cudaGetLastError() == cudaSuccess ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- cuBLASLt
+constexpr int kMaxDevices = 64;
+cublasLtHandle_t g_lt[kMaxDevices];
+std::atomic<int> g_gemm_mode{0};   // 0: emulated FP32 where offered, 1: plain FP32 only
+std::mutex g_lt_mu;
+
+int lt_handle(cublasLtHandle_t* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_lt_mu);
+    if (!g_lt[dev] && cublasLtCreate(&g_lt[dev]) != CUBLAS_STATUS_SUCCESS) return SRWM_ERR_CUDA;
+    *out = g_lt[dev];
+    return SRWM_OK;
+}
+
+// Row-major Out[N, M] = epilogue(X[N, K] Wt^T + bias) (+ C when accumulate),
+// with W stored row-major [M, K] as a PyTorch Linear weight.  In cuBLASLt's
+// column-major terms this is Out^T[M, N] = op(W)[M, K] X^T[K, N]: A = W with
+// transa = T (its column-major view is W^T), B = X untransposed.
+struct LtGuard {
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    ~LtGuard()
+    {
+        if (pref) cublasLtMatmulPreferenceDestroy(pref);
+        if (c) cublasLtMatrixLayoutDestroy(c);
+        if (b) cublasLtMatrixLayoutDestroy(b);
+        if (a) cublasLtMatrixLayoutDestroy(a);
+        if (op) cublasLtMatmulDescDestroy(op);
+    }
+};
+
+// One product with a given compute type; SRWM_ERR_UNSUPPORTED when cuBLASLt
+// offers no algorithm for it.
+int linear_with(cublasLtHandle_t lt, cublasComputeType_t compute, const float* X, const float* W, const float* bias,
+                float* out, long long N, int K, int M, bool relu, bool accumulate, void* ws, size_t ws_bytes,
+                cudaStream_t st)
+{
+    LtGuard gd;
+    const cublasOperation_t tA = CUBLAS_OP_T, tB = CUBLAS_OP_N;
+    const cublasLtEpilogue_t epi = relu ? CUBLASLT_EPILOGUE_RELU_BIAS : CUBLASLT_EPILOGUE_BIAS;
+    if (cublasLtMatmulDescCreate(&gd.op, compute, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) return SRWM_ERR_UNSUPPORTED;
+    if (cublasLtMatmulDescSetAttribute(gd.op, CUBLASLT_MATMUL_DESC_TRANSA, &tA, sizeof(tA)) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescSetAttribute(gd.op, CUBLASLT_MATMUL_DESC_TRANSB, &tB, sizeof(tB)) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescSetAttribute(gd.op, CUBLASLT_MATMUL_DESC_EPILOGUE, &epi, sizeof(epi)) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescSetAttribute(gd.op, CUBLASLT_MATMUL_DESC_BIAS_POINTER, &bias, sizeof(bias)) !=
+            CUBLAS_STATUS_SUCCESS)
+        return SRWM_ERR_CUDA;
+    if (cublasLtMatrixLayoutCreate(&gd.a, CUDA_R_32F, K, M, K) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&gd.b, CUDA_R_32F, K, static_cast<uint64_t>(N), K) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&gd.c, CUDA_R_32F, M, static_cast<uint64_t>(N), M) != CUBLAS_STATUS_SUCCESS)
+        return SRWM_ERR_CUDA;
+    if (cublasLtMatmulPreferenceCreate(&gd.pref) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulPreferenceSetAttribute(gd.pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
+                                             sizeof(ws_bytes)) != CUBLAS_STATUS_SUCCESS)
+        return SRWM_ERR_CUDA;
+    cublasLtMatmulHeuristicResult_t heur;
+    int found = 0;
+    if (cublasLtMatmulAlgoGetHeuristic(lt, gd.op, gd.a, gd.b, gd.c, gd.c, gd.pref, 1, &heur, &found) !=
+            CUBLAS_STATUS_SUCCESS ||
+        found < 1)
+        return SRWM_ERR_UNSUPPORTED;
+    const float alpha = 1.f, beta = accumulate ? 1.f : 0.f;
+    if (cublasLtMatmul(lt, gd.op, &alpha, W, gd.a, X, gd.b, &beta, out, gd.c, out, gd.c, &heur.algo, ws, ws_bytes,
+                       st) != CUBLAS_STATUS_SUCCESS)
+        return SRWM_ERR_CUDA;
+    return SRWM_OK;
+}
+
+// fp32 GEMM: unless plain FP32 is forced (srwm_debug_set_layer_gemm), first as FP32 emulated on the BF16 tensor cores (each fp32
+// input split into three BF16 parts, the nine partial products accumulated in
+// fp32: fp32-level accuracy), else, where cuBLASLt offers no such algorithm
+// for this shape and epilogue, in plain FP32.
+int linear(cublasLtHandle_t lt, const float* X, const float* W, const float* bias, float* out, long long N, int K,
+           int M, bool relu, bool accumulate, void* ws, size_t ws_bytes, cudaStream_t st)
+{
+    if (N == 0) return SRWM_OK;
+    int rc = SRWM_ERR_UNSUPPORTED;
+    if (g_gemm_mode == 0)
+        rc = linear_with(lt, CUBLAS_COMPUTE_32F_EMULATED_16BFX9, X, W, bias, out, N, K, M, relu, accumulate, ws,
+                         ws_bytes, st);
+    if (rc == SRWM_ERR_UNSUPPORTED)
+        rc = linear_with(lt, CUBLAS_COMPUTE_32F, X, W, bias, out, N, K, M, relu, accumulate, ws, ws_bytes, st);
+    return rc;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct LayerWs {
+    size_t a, y, f, wf, cnt, lt, total;
+};
+
+// Workspace regions (each 256-byte aligned): a = LN1(u), later LN2(h);
+// y = SRWM output; f = feed-forward hidden; the SRWM's final state and
+// schedule counters; cuBLASLt scratch.
+bool layer_ws(long long B, long long T, long long H, long long d, long long n_lr, long long d_ff, LayerWs* w)
+{
+    const long long N = B * T, D = H * d, m = 3 * d + n_lr;
+    if (N < 0 || D <= 0 || N > (1LL << 40) / (D > d_ff ? D : d_ff)) return false;
+    w->a = 0;
+    w->y = w->a + align256(static_cast<size_t>(N * D) * 4);
+    w->f = w->y + align256(static_cast<size_t>(N * D) * 4);
+    w->wf = w->f + align256(static_cast<size_t>(N * d_ff) * 4);
+    w->cnt = w->wf + align256(static_cast<size_t>(B * H * m * d) * 4);
+    w->lt = w->cnt + align256(static_cast<size_t>(B * H) * 4);
+    w->total = w->lt + kLtWorkspace;
+    return true;
+}
+
+int check_device(const void* p)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_NOT_DEVICE;
+    }
+    return (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) ? SRWM_OK
+                                                                                       : SRWM_ERR_NOT_DEVICE;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t srwm_layer_workspace_bytes(int B, int T, int H, int d, int n_lr, int d_ff)
+{
+    if (B <= 0 || T < 0 || H <= 0 || (d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4) || d_ff <= 0 ||
+        d_ff % 4 != 0 || static_cast<long long>(H) * d > 1024)
+        return 0;
+    LayerWs w;
+    if (!layer_ws(B, T, H, d, n_lr, d_ff, &w)) return 0;
+    return w.total;
+}
+
+int srwm_layer_forward(const float* u, int B, int T, int H, int d, int n_lr, int softmax_input,
+                       const float* ln1_gamma, const float* ln1_beta, const float* W0, const float* ln2_gamma,
+                       const float* ln2_beta, const float* W1, const float* b1, int d_ff, const float* W2,
+                       const float* b2, float* out, float* W_final, void* workspace, size_t workspace_bytes,
+                       void* stream)
+{
+    if (!ln1_gamma || !ln1_beta || !W0 || !ln2_gamma || !ln2_beta || !W1 || !b1 || !W2 || !b2 || !workspace ||
+        (T > 0 && (!u || !out)))
+        return SRWM_ERR_NULL;
+    if (B <= 0 || H <= 0 || T < 0 || d_ff <= 0) return SRWM_ERR_SHAPE;
+    if ((d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4) || (softmax_input != 0 && softmax_input != 1) ||
+        d_ff % 4 != 0 || static_cast<long long>(H) * d > 1024)
+        return SRWM_ERR_UNSUPPORTED;
+    LayerWs w;
+    if (!layer_ws(B, T, H, d, n_lr, d_ff, &w)) return SRWM_ERR_SHAPE;
+    if (workspace_bytes < w.total) return SRWM_ERR_SHAPE;
+    const long long N = static_cast<long long>(B) * T, D = static_cast<long long>(H) * d;
+    const long long m = 3LL * d + n_lr;
+    const void* ptrs[] = {u, ln1_gamma, ln1_beta, W0, ln2_gamma, ln2_beta, W1, b1, W2, b2, out, W_final, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SRWM_ERR_ALIGN;
+    // the outputs and the workspace overlap no input and no other output
+    const size_t nu = static_cast<size_t>(N * D) * 4, nwf = static_cast<size_t>(B * H * m * d) * 4;
+    const size_t nD = static_cast<size_t>(D) * 4, nW0 = static_cast<size_t>(H * m * d) * 4;
+    const size_t nW1 = static_cast<size_t>(d_ff) * static_cast<size_t>(D) * 4, nb1 = static_cast<size_t>(d_ff) * 4;
+    const std::pair<const void*, size_t> ins[] = {{u, nu},         {ln1_gamma, nD}, {ln1_beta, nD}, {W0, nW0},
+                                                  {ln2_gamma, nD}, {ln2_beta, nD},  {W1, nW1},      {b1, nb1},
+                                                  {W2, nW1},       {b2, nD}};
+    for (const auto& in : ins) {
+        if (overlaps(out, nu, in.first, in.second) || overlaps(workspace, w.total, in.first, in.second) ||
+            overlaps(W_final, nwf, in.first, in.second))
+            return SRWM_ERR_ALIAS;
+    }
+    if (overlaps(out, nu, workspace, w.total) || overlaps(W_final, nwf, workspace, w.total) ||
+        overlaps(out, nu, W_final, nwf))
+        return SRWM_ERR_ALIAS;
+    for (const void* p : ptrs) {
+        if (!p || (T == 0 && (p == u || p == out))) continue;
+        const int rc = check_device(p);
+        if (rc != SRWM_OK) return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(workspace);
+    float* a = reinterpret_cast<float*>(base + w.a);
+    float* y = reinterpret_cast<float*>(base + w.y);
+    float* f = reinterpret_cast<float*>(base + w.f);
+    float* wf = W_final ? W_final : reinterpret_cast<float*>(base + w.wf);
+    int* cnt = reinterpret_cast<int*>(base + w.cnt);
+    void* ltws = base + w.lt;
+
+    int rc;
+    if ((rc = launch_ln(false, u, nullptr, nullptr, ln1_gamma, ln1_beta, a, N, static_cast<int>(D), st)) != SRWM_OK)
+        return rc;
+    if ((rc = srwm_forward_balanced(T > 0 ? a : nullptr, W0, B, T, H, d, n_lr, softmax_input, T > 0 ? y : nullptr, wf,
+                                    cnt, static_cast<size_t>(B) * H * 4, stream)) != SRWM_OK)
+        return rc;
+    if (T == 0) return SRWM_OK;
+    // h = u + y goes to out (the second product accumulates onto it); LN2(h) reuses a
+    if ((rc = launch_ln(true, u, y, out, ln2_gamma, ln2_beta, a, N, static_cast<int>(D), st)) != SRWM_OK) return rc;
+    cublasLtHandle_t lt;
+    if ((rc = lt_handle(&lt)) != SRWM_OK) return rc;
+    if ((rc = linear(lt, a, W1, b1, f, N, static_cast<int>(D), d_ff, true, false, ltws, kLtWorkspace, st)) != SRWM_OK)
+        return rc;
+    return linear(lt, f, W2, b2, out, N, d_ff, static_cast<int>(D), false, true, ltws, kLtWorkspace, st);
+}
+
+int srwm_debug_set_layer_gemm(int plain_fp32)
+{
+    if (plain_fp32 != 0 && plain_fp32 != 1) return SRWM_ERR_UNSUPPORTED;
+    g_gemm_mode.store(plain_fp32);
+    return SRWM_OK;
+}
+
+}  // extern "C"

@@ -38,7 +38,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22  # normal pairs per chunk: bounds the temporaries to ~100 MB
 
 # One tag per drawn quantity.
-TAG_X, TAG_W0, TAG_MU, TAG_LABELS, TAG_DY, TAG_DWF = 1, 2, 3, 4, 5, 6
+TAG_X, TAG_W0, TAG_MU, TAG_LABELS, TAG_DY, TAG_DWF, TAG_LAYER = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclasses.dataclass(frozen=True)
@@ -160,6 +160,37 @@ def make_cotangents(wl: Workload, with_dW_final: bool = True):
     if with_dW_final:
         dWf = normals(stream_key(wl.seed, TAG_DWF), B * H * m * d).reshape(B, H, m, d)
     return dy, dWf
+
+
+def make_layer_params(H: int, d: int, n_lr: int, d_ff: int, seed: int) -> dict:
+    """Seeded float32 parameters of one Recursive Self-Transformer layer:
+    layer-norm scales ~ 1 + N(0, 0.1^2) and shifts ~ N(0, 0.1^2), W0 ~ N(0, 1/d)
+    per head, feed-forward weights ~ N(0, 1/fan_in) and biases ~ N(0, 0.1^2)."""
+    D = H * d
+    key = stream_key(seed, TAG_LAYER)
+    sizes = [("ln1_gamma", (D,)), ("ln1_beta", (D,)), ("ln2_gamma", (D,)), ("ln2_beta", (D,)),
+             ("W1", (d_ff, D)), ("b1", (d_ff,)), ("W2", (D, d_ff)), ("b2", (D,))]
+    total = sum(int(np.prod(s)) for _, s in sizes)
+    z = normals(key, total)
+    out, off = {}, 0
+    for name, shape in sizes:
+        n = int(np.prod(shape))
+        v = z[off:off + n].reshape(shape).astype(np.float64)
+        off += n
+        if name.endswith("gamma"):
+            v = 1.0 + 0.1 * v
+        elif name in ("W1", "W2"):
+            v = v / np.sqrt(shape[1])
+        else:
+            v = 0.1 * v
+        out[name] = np.ascontiguousarray(v.astype(np.float32))
+    out["W0"] = make_W0(H, d, n_lr, seed)
+    return out
+
+
+def make_layer_input(B: int, T: int, D: int, seed: int) -> np.ndarray:
+    """Layer input tokens u [B, T, D] float32 ~ N(0, 1)."""
+    return normals(stream_key(seed, TAG_X), B * T * D).reshape(B, T, D)
 
 
 def workload(name: str, **overrides) -> Workload:

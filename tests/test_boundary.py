@@ -182,3 +182,36 @@ def test_backward_validation(lib):
     assert bwd(dx=A + 0x3000004) == 4       # misaligned
     assert bwd(dx=A + 0x2000000) == 5       # dx on top of dy
     assert bwd(ws=A) == 5                   # workspace over x
+
+
+def test_layer_workspace_and_validation(lib):
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.srwm_layer_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.srwm_layer_workspace_bytes.restype = SZ
+    lib.srwm_layer_forward.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P, SZ, P]
+    ws = lib.srwm_layer_workspace_bytes
+    assert ws(2, 10, 2, 16, 4, 128) > 32 << 20          # activations plus the GEMM scratch
+    assert ws(2, 10, 2, 16, 4, 130) == 0                # d_ff % 4 != 0
+    assert ws(2, 10, 32, 64, 4, 128) == 0               # D = 2048 > 1024
+    assert ws(2, 10, 2, 48, 4, 128) == 0                # d unsupported
+    grow = ws(2, 20, 2, 16, 4, 128) - ws(2, 10, 2, 16, 4, 128)
+    assert grow >= 2 * 10 * (2 * 2 * 16 + 128) * 4      # a, y and the hidden layer scale with B*T
+
+    base = 0x100000
+    args = dict(u=base, B=2, T=3, H=2, d=16, n_lr=4, smx=0, g1=base + 0x10000, be1=base + 0x20000,
+                W0=base + 0x30000, g2=base + 0x40000, be2=base + 0x50000, W1=base + 0x60000, b1=base + 0x70000,
+                d_ff=64, W2=base + 0x80000, b2=base + 0x90000, out=base + 0xA0000, Wf=None, ws=base + 0x1000000,
+                ws_bytes=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.srwm_layer_forward(a["u"], a["B"], a["T"], a["H"], a["d"], a["n_lr"], a["smx"], a["g1"], a["be1"],
+                                      a["W0"], a["g2"], a["be2"], a["W1"], a["b1"], a["d_ff"], a["W2"], a["b2"],
+                                      a["out"], a["Wf"], a["ws"], a["ws_bytes"], None)
+
+    assert call(u=None) == 1 and call(W1=None) == 1 and call(ws=None) == 1
+    assert call(B=0) == 2 and call(T=-1) == 2
+    assert call(d=48) == 3 and call(d_ff=66) == 3 and call(H=32, d=64) == 3
+    assert call(ws_bytes=1024) == 2
+    assert call(out=base + 0xA0004) == 4
+    assert call(out=base) == 5                          # out over u
