@@ -328,21 +328,20 @@ def main():
     value = world * ht_per_step * args.steps / t_max
     ms_per_step = 1e3 * t_max / args.steps
 
-    # ---------------- end to end through the public API with host buffers
+    # ---------------- end to end through the public API with host buffers:
+    # srwm_forward_host copies x and W0 in and y and W_final out, overlapping
+    # the copies with the recurrence chunk by chunk
     x_h = torch.from_numpy(x_np).pin_memory()
     W0_h = torch.from_numpy(W0_np).pin_memory()
     y_h = torch.empty(x_h.shape, dtype=torch.float32).pin_memory()
     Wf_h = torch.empty(tuple(Wf.shape), dtype=torch.float32).pin_memory()
-    xd = torch.empty_like(x)
-    W0d = torch.empty_like(W0)
+    chunk = 128
+    host_ws = torch.empty(binding.srwm_forward_host_workspace_bytes(wl.B, wl.T, wl.H, wl.d, wl.n_lr, chunk),
+                          dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        xd.copy_(x_h, non_blocking=True)
-        W0d.copy_(W0_h, non_blocking=True)
-        binding.srwm_forward_balanced(xd, W0d, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf,
-                                      workspace=workspace, stream=stream)
-        y_h.copy_(y, non_blocking=True)
-        Wf_h.copy_(Wf, non_blocking=True)
+        binding.srwm_forward_host(x_h, W0_h, wl.n_lr, wl.softmax_input, y_out=y_h, W_final=Wf_h, chunk_steps=chunk,
+                                  workspace=host_ws, stream=stream)
 
     for _ in range(2):
         e2e_step()
@@ -358,10 +357,11 @@ def main():
     e2e = {"value": world * ht_per_step * args.e2e_steps / t_e2e, "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * 4 + W0_h.numel() * 4,
            "d2h_bytes_per_step": y_h.numel() * 4 + Wf_h.numel() * 4,
-           "ms_per_step": 1e3 * t_e2e / args.e2e_steps}
-    # the e2e outputs are the device outputs
-    if not torch.equal(y_h, y.cpu()):
-        raise RuntimeError("e2e copy-back mismatch")
+           "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "api": f"srwm_forward_host (chunks of {chunk} steps)"}
+    # the host results agree with the device path's (chunk restarts change fp32 rounding only)
+    y_dev = y.cpu()
+    if float((y_h - y_dev).abs().max()) > 1e-4 * float(y_dev.abs().max()):
+        raise RuntimeError("e2e host results differ from the device results")
 
     # ---------------- FMA probe (calibration of the FP32 roofline)
     props = torch.cuda.get_device_properties(dev)

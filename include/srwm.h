@@ -139,6 +139,37 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
                       int softmax_input, float* y_out, float* W_final, void* stream);
 
 /*
+ * srwm_forward_host -- srwm_forward with HOST buffers: x, W0 in host memory,
+ * y and W_final written to host memory.  The copies overlap the recurrence:
+ * the sequence is cut into chunks of chunk_steps steps (<= 0: 128).  The H2D
+ * copy of chunk k+1 and the D2H copy of chunk k-1 run on the library's own copy
+ * streams while chunk k runs on `stream`, the state passing between chunks as
+ * in srwm_forward_from.  Results equal srwm_forward's within fp32 rounding (a
+ * chunk restarts its first read-out from the stored state).
+ *
+ *   x_host        [B, T, H, d]  host memory, page-locked (cudaHostAlloc /
+ *                 cudaHostRegister) for the copies to overlap; pageable works
+ *                 but copies synchronously
+ *   W0_host       [H, m, d]     host memory
+ *   y_host        [B, T, H, d]  host memory, written
+ *   W_final_host  [B, H, m, d]  host memory, written
+ *   chunk_steps   steps per chunk
+ *   workspace     DEVICE scratch of srwm_forward_host_workspace_bytes(...)
+ *                 bytes, 16-byte aligned
+ *
+ * Everything is enqueued on `stream`: once it has completed (e.g. after
+ * cudaStreamSynchronize), the host outputs are written.  Host buffers and the
+ * workspace must stay valid and untouched until then.  The copy streams and
+ * events are created on a device's first call and kept until the process
+ * exits; calls on one device are enqueued one at a time.  Returns
+ * SRWM_ERR_UNSUPPORTED when a "host" pointer is device or managed memory.
+ */
+size_t srwm_forward_host_workspace_bytes(int B, int T, int H, int d, int n_lr, int chunk_steps);
+int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, int H, int d, int n_lr,
+                      int softmax_input, float* y_host, float* W_final_host, int chunk_steps,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * srwm_step -- one step of the same recurrence from a per-sequence state:
  * W_out[b,h] = W_in[b,h] + update, y_t[b,h] = y from W_in[b,h].  Calling it T
  * times, feeding W_out back as W_in, reproduces srwm_forward.

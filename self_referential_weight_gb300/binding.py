@@ -19,7 +19,8 @@ SRWM_OK = 0
 SRWM_ERR_TIMEOUT = 7
 
 EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noalloc",
-           "srwm_forward_workspace_bytes", "srwm_forward_from",
+           "srwm_forward_workspace_bytes", "srwm_forward_from", "srwm_forward_host",
+           "srwm_forward_host_workspace_bytes",
            "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes",
            "srwm_layer_forward", "srwm_layer_workspace_bytes", "srwm_debug_set_layer_gemm", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
            "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
@@ -59,6 +60,10 @@ def _lib():
         lib.srwm_debug_set_segment_len.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward_from.restype = I
+        lib.srwm_forward_host.argtypes = [P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]
+        lib.srwm_forward_host.restype = I
+        lib.srwm_forward_host_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.srwm_forward_host_workspace_bytes.restype = SZ
         lib.srwm_step.argtypes = [P, P, I, I, I, I, I, P, P, P]
         lib.srwm_step.restype = I
         lib.srwm_backward.argtypes = [P, P, I, I, I, I, I, I, P, P, P, P, P, SZ, P]
@@ -196,6 +201,43 @@ def srwm_forward_from(x, W_init, n_lr, softmax_input=False, y_out=None, W_final=
                                   int(n_lr), int(bool(softmax_input)), _dev(y_out, "y_out", (B, T, H, d)),
                                   _dev(W_final, "W_final", (B, H, m, d)), _stream_handle(stream))
     _check(rc, "srwm_forward_from")
+    return y_out, W_final
+
+
+def _host(t, name, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CPU tensor (pinned for overlapped copies)")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else 0)
+
+
+def srwm_forward_host_workspace_bytes(B, T, H, d, n_lr, chunk_steps=0) -> int:
+    return int(_lib().srwm_forward_host_workspace_bytes(int(B), int(T), int(H), int(d), int(n_lr), int(chunk_steps)))
+
+
+def srwm_forward_host(x, W0, n_lr, softmax_input=False, y_out=None, W_final=None, chunk_steps=0, workspace=None,
+                      stream=None):
+    """srwm_forward on host tensors (x [B,T,H,d], W0 [H,m,d], pinned for overlap):
+    the copies to and from the device overlap the recurrence.  Returns
+    (y, W_final) host tensors, written once `stream` has completed."""
+    B, T, H, d = x.shape
+    m = 3 * d + n_lr
+    if y_out is None:
+        y_out = torch.empty((B, T, H, d), dtype=torch.float32).pin_memory()
+    if W_final is None:
+        W_final = torch.empty((B, H, m, d), dtype=torch.float32).pin_memory()
+    if workspace is None:
+        need = srwm_forward_host_workspace_bytes(B, T, H, d, n_lr, chunk_steps)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    rc = _lib().srwm_forward_host(_host(x, "x"), _host(W0, "W0", (H, m, d)), B, T, H, d, int(n_lr),
+                                  int(bool(softmax_input)), _host(y_out, "y_out", (B, T, H, d)),
+                                  _host(W_final, "W_final", (B, H, m, d)), int(chunk_steps),
+                                  ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "srwm_forward_host")
     return y_out, W_final
 
 

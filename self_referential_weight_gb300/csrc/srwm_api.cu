@@ -295,6 +295,91 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
     return launch(li, tx, ty, kp, pairs, static_cast<int>(need < ctas ? need : ctas), stream);
 }
 
+
+// ---------------------------------------------------------------- host pipeline
+// Copy streams and events of srwm_forward_host, created once per device and
+// reused; a mutex serialises the enqueueing of concurrent calls on a device.
+constexpr int kPipeSlots = 3;
+struct Pipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start, w0, end, in[kPipeSlots], comp[kPipeSlots], out[kPipeSlots];
+    std::mutex mu;
+};
+constexpr int kPipeDevices = 64;
+Pipe g_pipe[kPipeDevices];
+std::mutex g_pipe_init_mu;
+
+int pipe_for_device(Pipe** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kPipeDevices) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_pipe_init_mu);
+    Pipe& p = g_pipe[dev];
+    if (!p.ready) {
+        bool ok = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking) == cudaSuccess;
+        cudaEvent_t* evs[] = {&p.start, &p.w0, &p.end};
+        for (cudaEvent_t* e : evs) ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < kPipeSlots; ++i) {
+            ok = ok && cudaEventCreateWithFlags(&p.in[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p.comp[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p.out[i], cudaEventDisableTiming) == cudaSuccess;
+        }
+        if (!ok) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        p.ready = true;
+    }
+    *out = &p;
+    return SRWM_OK;
+}
+
+// Host memory (pinned or pageable), not device or managed memory.
+int check_host_ptr(const void* ptr)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_UNSUPPORTED;
+    }
+    return (attr.type == cudaMemoryTypeHost || attr.type == cudaMemoryTypeUnregistered) ? SRWM_OK
+                                                                                        : SRWM_ERR_UNSUPPORTED;
+}
+
+struct HostWs {
+    size_t w0, state, cnt, x[kPipeSlots], y[kPipeSlots], total;
+};
+
+bool host_ws(long long B, long long T, long long H, long long d, long long n_lr, long long C, HostWs* w)
+{
+    const long long m = 3 * d + n_lr;
+    auto a256 = [](size_t n) { return (n + 255) / 256 * 256; };
+    const size_t chunk = a256(static_cast<size_t>(B * C * H * d) * 4);
+    size_t off = 0;
+    w->w0 = off;
+    off += a256(static_cast<size_t>(H * m * d) * 4);
+    w->state = off;
+    off += a256(static_cast<size_t>(B * H * m * d) * 4);
+    w->cnt = off;
+    off += a256(static_cast<size_t>(B * H) * 4);
+    for (int i = 0; i < kPipeSlots; ++i) {
+        w->x[i] = off;
+        off += chunk;
+        w->y[i] = off;
+        off += chunk;
+    }
+    w->total = off;
+    (void)T;
+    return true;
+}
+
+int effective_chunk(int T, int chunk_steps) { return chunk_steps > 0 ? (chunk_steps < T ? chunk_steps : (T > 0 ? T : 1)) : (T < 128 ? (T > 0 ? T : 1) : 128); }
+
 }  // namespace
 
 extern "C" {
@@ -426,6 +511,97 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
         return SRWM_ERR_CUDA;
     }
     return srwm::launch_sum_over_batch(dW_seq, dW0, B, per_batch, st) == 0 ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+size_t srwm_forward_host_workspace_bytes(int B, int T, int H, int d, int n_lr, int chunk_steps)
+{
+    if (check_params(B, T, H, d, n_lr, 0) != SRWM_OK) return 0;
+    HostWs w;
+    host_ws(B, T, H, d, n_lr, effective_chunk(T, chunk_steps), &w);
+    return w.total;
+}
+
+int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, int H, int d, int n_lr,
+                      int softmax_input, float* y_host, float* W_final_host, int chunk_steps, void* workspace,
+                      size_t workspace_bytes, void* stream)
+{
+    if (!W0_host || !W_final_host || !workspace || (T > 0 && (!x_host || !y_host))) return SRWM_ERR_NULL;
+    int rc = check_params(B, T, H, d, n_lr, softmax_input);
+    if (rc != SRWM_OK) return rc;
+    const int C = effective_chunk(T, chunk_steps);
+    HostWs w;
+    host_ws(B, T, H, d, n_lr, C, &w);
+    if (workspace_bytes < w.total) return SRWM_ERR_SHAPE;
+    if (!aligned16(workspace)) return SRWM_ERR_ALIGN;
+    if ((rc = check_device_ptr(workspace)) != SRWM_OK) return rc;
+    const long long m = 3LL * d + n_lr;
+    const size_t nx = static_cast<size_t>(B) * T * H * d * 4, nwf = static_cast<size_t>(B) * H * m * d * 4;
+    if (T > 0 && (overlaps(y_host, nx, x_host, nx) || overlaps(y_host, nx, W0_host, static_cast<size_t>(H * m * d) * 4) ||
+                  overlaps(y_host, nx, W_final_host, nwf) || overlaps(W_final_host, nwf, x_host, nx)))
+        return SRWM_ERR_ALIAS;
+    const void* hosts[] = {x_host, W0_host, y_host, W_final_host};
+    for (const void* hp : hosts) {
+        if (!hp) continue;
+        if ((rc = check_host_ptr(hp)) != SRWM_OK) return rc;
+    }
+    Pipe* pp = nullptr;
+    if ((rc = pipe_for_device(&pp)) != SRWM_OK) return rc;
+    Pipe& P = *pp;
+    std::lock_guard<std::mutex> lk(P.mu);
+    cudaStream_t sc = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(workspace);
+    float* W0d = reinterpret_cast<float*>(base + w.w0);
+    float* S = reinterpret_cast<float*>(base + w.state);
+    int* cnt = reinterpret_cast<int*>(base + w.cnt);
+    const size_t row = static_cast<size_t>(H) * d * 4;   // one step of one sequence
+    auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+
+    // the copy streams start after the work already on the caller's stream
+    if (fail(cudaEventRecord(P.start, sc)) || fail(cudaStreamWaitEvent(P.s_in, P.start, 0)) ||
+        fail(cudaStreamWaitEvent(P.s_out, P.start, 0)) ||
+        fail(cudaMemcpyAsync(W0d, W0_host, static_cast<size_t>(H * m * d) * 4, cudaMemcpyHostToDevice, P.s_in)) ||
+        fail(cudaEventRecord(P.w0, P.s_in)) || fail(cudaStreamWaitEvent(sc, P.w0, 0))) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    if (T == 0) {
+        if ((rc = run(nullptr, W0d, 0, B, 0, H, d, n_lr, softmax_input, nullptr, S, sc)) != SRWM_OK) return rc;
+    }
+    const int K = T > 0 ? (T + C - 1) / C : 0;
+    for (int k = 0; k < K; ++k) {
+        const int slot = k % kPipeSlots, t0 = k * C, Ck = (T - t0 < C) ? T - t0 : C;
+        float* xb = reinterpret_cast<float*>(base + w.x[slot]);
+        float* yb = reinterpret_cast<float*>(base + w.y[slot]);
+        // x chunk k: host [B, T, H, d] rows t0 .. t0+Ck-1 -> contiguous [B, Ck, H, d]
+        if ((k >= kPipeSlots && fail(cudaStreamWaitEvent(P.s_in, P.comp[slot], 0))) ||
+            fail(cudaMemcpy2DAsync(xb, Ck * row, reinterpret_cast<const char*>(x_host) + t0 * row, T * row, Ck * row,
+                                   B, cudaMemcpyHostToDevice, P.s_in)) ||
+            fail(cudaEventRecord(P.in[slot], P.s_in)) || fail(cudaStreamWaitEvent(sc, P.in[slot], 0)) ||
+            (k >= kPipeSlots && fail(cudaStreamWaitEvent(sc, P.out[slot], 0)))) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        // the recurrence on chunk k, carrying the state in S (in place after the first chunk)
+        if ((rc = run(xb, k == 0 ? W0d : S, k == 0 ? 0 : 1, B, Ck, H, d, n_lr, softmax_input, yb, S, sc, cnt,
+                      static_cast<size_t>(B) * H * 4)) != SRWM_OK)
+            return rc;
+        // y chunk k back to host rows t0 .. t0+Ck-1
+        if (fail(cudaEventRecord(P.comp[slot], sc)) || fail(cudaStreamWaitEvent(P.s_out, P.comp[slot], 0)) ||
+            fail(cudaMemcpy2DAsync(reinterpret_cast<char*>(y_host) + t0 * row, T * row, yb, Ck * row, Ck * row, B,
+                                   cudaMemcpyDeviceToHost, P.s_out)) ||
+            fail(cudaEventRecord(P.out[slot], P.s_out))) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+    }
+    // the final state, then the caller's stream waits for every copy
+    if (fail(cudaEventRecord(P.end, sc)) || fail(cudaStreamWaitEvent(P.s_out, P.end, 0)) ||
+        fail(cudaMemcpyAsync(W_final_host, S, nwf, cudaMemcpyDeviceToHost, P.s_out)) ||
+        fail(cudaEventRecord(P.end, P.s_out)) || fail(cudaStreamWaitEvent(sc, P.end, 0))) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return SRWM_OK;
 }
 
 int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, int d, int n_lr,
