@@ -201,15 +201,18 @@ int srwm_step(const float* x_t, const float* W_in, int B, int H, int d, int n_lr
  *   dW0       [H, m, d]       written: the sum over sequences b of each
  *                             stream's dL/dW0, summed in order of b
  *   workspace device scratch of at least srwm_backward_workspace_bytes(...)
- *             bytes, 16-byte aligned, contents irrelevant on entry; it holds
- *             the state W at the start of every 32-step segment and the
- *             per-stream dL/dW0.  It must stay untouched until the work on
- *             `stream` has finished.
+ *             bytes, 16-byte aligned, contents irrelevant on entry.  It holds
+ *             the forward's per-step records (phi(k), u, gates, a: about
+ *             4 * (5d + 4 + n_lr) bytes per step and stream), W_T, the
+ *             forward's y and the per-stream dL/dW0.  It must stay untouched
+ *             until the work on `stream` has finished.
  *
- * The forward is recomputed inside (one extra forward pass); y and W_final
- * are not needed.  T = 0 writes dW0 = sum_b dW_final (or zero).  The same
- * pointer rules as above apply; the workspace must not overlap anything else.
- * Returns SRWM_ERR_SHAPE when workspace_bytes is too small.
+ * The call runs the forward pass itself (with the records), then the steps
+ * backwards from W_T.  Each step recovers W_{t-1} by subtracting the recorded
+ * rank-one update.  y and W_final need not be passed in.  T = 0 writes
+ * dW0 = sum_b dW_final (or zero).  The same pointer rules as above apply; the
+ * workspace must not overlap anything else.  Returns SRWM_ERR_SHAPE when
+ * workspace_bytes is too small.
  */
 int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,
                   int softmax_input, const float* dy, const float* dW_final, float* dx, float* dW0,
@@ -217,8 +220,9 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
 
 /*
  * srwm_backward_workspace_bytes -- scratch size srwm_backward needs for these
- * sizes: 4 * B * H * m * d * ceil(T / 32) bytes (at least one segment),
- * rounded up to 256.  Returns 0 for unsupported or invalid sizes.
+ * sizes, the sum of 256-byte aligned regions: 2 x 4 B*H*m*d (dL/dW0 per
+ * stream, W_T), 4 B*T*H*d (y), 4 B*H*T*ceil4(5d + 4 + n_lr) (records),
+ * 4 B*H (counters).  Returns 0 for unsupported or invalid sizes.
  */
 size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr);
 

@@ -111,14 +111,14 @@ int make_stream_map(CUtensorMap* map, const float* base, int B, int T, int H, in
 }
 
 // The kernel for a call; at d = 64 it depends on the streams per SM.
-int info_for(int d, int n_lr, int smx, long long n_streams, srwm::LaunchInfo* li)
+int info_for(int d, int n_lr, int smx, long long n_streams, srwm::LaunchInfo* li, bool emit = false)
 {
     if (d == 16) {
-        *li = srwm::launch_info_d16(n_lr, smx);
+        *li = srwm::launch_info_d16(n_lr, smx, emit);
         return SRWM_OK;
     }
     if (d == 32) {
-        *li = srwm::launch_info_d32(n_lr, smx);
+        *li = srwm::launch_info_d32(n_lr, smx, emit);
         return SRWM_OK;
     }
     int dev = 0, n_sm = 0;
@@ -127,7 +127,7 @@ int info_for(int d, int n_lr, int smx, long long n_streams, srwm::LaunchInfo* li
         cudaGetLastError();
         return SRWM_ERR_CUDA;
     }
-    *li = srwm::launch_info_d64(n_lr, smx, n_streams, n_sm);
+    *li = srwm::launch_info_d64(n_lr, smx, n_streams, n_sm, emit);
     return SRWM_OK;
 }
 
@@ -219,7 +219,7 @@ int choose_seg_len(long long n_streams, int T, long long slots)
 // Shared body of srwm_forward (per_seq = 0) and srwm_step (per_seq = 1, T = 1).
 int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, int d, int n_lr,
         int smx, float* y, float* W_out, cudaStream_t stream, int* seg_done = nullptr,
-        size_t seg_done_bytes = 0)
+        size_t seg_done_bytes = 0, float* emit = nullptr, int emit_stride = 0)
 {
     const long long m = 3LL * d + n_lr;
     const size_t nx = static_cast<size_t>(B) * T * H * d * sizeof(float);
@@ -244,7 +244,7 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
     }
 
     srwm::LaunchInfo li;
-    if ((rc = info_for(d, n_lr, smx, static_cast<long long>(B) * H, &li)) != SRWM_OK) return rc;
+    if ((rc = info_for(d, n_lr, smx, static_cast<long long>(B) * H, &li, emit != nullptr)) != SRWM_OK) return rc;
     CUtensorMap tx, ty;
     std::memset(&tx, 0, sizeof(tx));
     std::memset(&ty, 0, sizeof(ty));
@@ -267,6 +267,8 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
     kp.seg_len = T > 0 ? T : 1;
     kp.n_items = kp.n_streams;
     kp.seg_done = nullptr;
+    kp.emit = emit;
+    kp.emit_stride = emit_stride;
     if (!seg_done) return launch(li, tx, ty, kp, pairs, 0, stream);
 
     // Balanced schedule: streams cut into segments, a persistent cooperative
@@ -431,14 +433,44 @@ int srwm_debug_set_segment_len(int steps)
     return SRWM_OK;
 }
 
+namespace {
+
+// srwm_backward's workspace, each region 256-byte aligned: dL/dW0 per stream,
+// W_T, the forward's y (not needed, but the forward kernels write it), the
+// per-step records, the schedule counters.
+struct BwdWs {
+    size_t dws, wt, y, rec, cnt, total;
+};
+
+bool bwd_ws(long long B, long long T, long long H, long long d, long long n_lr, BwdWs* w)
+{
+    const long long m = 3 * d + n_lr, streams = B * H;
+    auto a256 = [](size_t n) { return (n + 255) / 256 * 256; };
+    const size_t md = static_cast<size_t>(m * d) * 4;
+    size_t off = 0;
+    w->dws = off;
+    off += a256(static_cast<size_t>(streams) * md);
+    w->wt = off;
+    off += a256(static_cast<size_t>(streams) * md);
+    w->y = off;
+    off += a256(static_cast<size_t>(B * T * H * d) * 4);
+    w->rec = off;
+    off += a256(static_cast<size_t>(streams * T) * srwm::emit_record_floats(static_cast<int>(d), static_cast<int>(n_lr)) * 4);
+    w->cnt = off;
+    off += a256(static_cast<size_t>(streams) * 4);
+    w->total = off;
+    return true;
+}
+
+}  // namespace
+
 size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr)
 {
     if (B <= 0 || H <= 0 || T < 0 || (d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4)) return 0;
-    const size_t md = static_cast<size_t>(3 * d + n_lr) * d;
-    const size_t streams = static_cast<size_t>(B) * H;
-    const size_t nseg = T > 0 ? static_cast<size_t>((T + 31) / 32) : 1;
-    const size_t floats = streams * md * nseg;   // dL/dW0 per stream + states of segments 1..
-    return (floats * sizeof(float) + 255) / 256 * 256;
+    if (check_params(B, T, H, d, n_lr, 0) != SRWM_OK) return 0;
+    BwdWs w;
+    bwd_ws(B, T, H, d, n_lr, &w);
+    return w.total;
 }
 
 int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr, int softmax_input,
@@ -473,7 +505,10 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
         if ((rc = check_device_ptr(devs[i])) != SRWM_OK) return rc;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* dW_seq = static_cast<float*>(workspace);
+    BwdWs w;
+    bwd_ws(B, T, H, d, n_lr, &w);
+    char* base = static_cast<char*>(workspace);
+    float* dW_seq = reinterpret_cast<float*>(base + w.dws);
     const size_t per_batch = static_cast<size_t>(H) * m * d;
     if (T == 0) {
         // dL/dW0 = sum over b of dL/dW_final (W_final = W0 for every b)
@@ -486,6 +521,14 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
         }
         return srwm::launch_sum_over_batch(dW_final, dW0, B, per_batch, st) == 0 ? SRWM_OK : SRWM_ERR_CUDA;
     }
+    // 1. the forward pass with its per-step records and W_T
+    float* WT = reinterpret_cast<float*>(base + w.wt);
+    float* rec = reinterpret_cast<float*>(base + w.rec);
+    const int stride = srwm::emit_record_floats(d, n_lr);
+    if ((rc = run(x, W0, 0, B, T, H, d, n_lr, softmax_input, reinterpret_cast<float*>(base + w.y), WT, st,
+                  reinterpret_cast<int*>(base + w.cnt), static_cast<size_t>(B) * H * 4, rec, stride)) != SRWM_OK)
+        return rc;
+    // 2. the steps backwards, one CTA per stream
     const srwm::BwdLaunch li = srwm::bwd_info(d, n_lr);
     if (cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, li.smem_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -493,12 +536,13 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
     }
     srwm::BwdParams bp;
     bp.x = x;
-    bp.W0 = W0;
+    bp.WT = WT;
+    bp.rec = rec;
+    bp.rec_stride = stride;
     bp.dy = dy;
     bp.dWf = dW_final;
     bp.dx = dx;
     bp.dW_seq = dW_seq;
-    bp.snap = dW_seq + static_cast<size_t>(B) * per_batch;
     bp.B = B;
     bp.T = T;
     bp.H = H;
@@ -510,6 +554,7 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
         cudaGetLastError();
         return SRWM_ERR_CUDA;
     }
+    // 3. dL/dW0 = sum over sequences, in order of b
     return srwm::launch_sum_over_batch(dW_seq, dW0, B, per_batch, st) == 0 ? SRWM_OK : SRWM_ERR_CUDA;
 }
 

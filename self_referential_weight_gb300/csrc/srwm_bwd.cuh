@@ -16,15 +16,15 @@
 // (and dx = x~ (dx~ - <x~, dx~>) when the input goes through softmax).
 //
 // Memory: the pages name "memory-efficient" backpropagation through time
-// without details.  Here the state W is kept only at the start of every
-// KSEG-step segment (phase 1 recomputes the forward once and stores those
-// states in the workspace); phase 2 walks the segments backwards, recomputes
-// each one from its stored start, records per step phi(k), u, the gates, a and
-// x~ in shared memory, and then steps back through it.  Stepping back
-// subtracts exactly the update that the recompute added, so no matrix
-// inversion (which would amplify rounding wherever the update contracts W) is
-// needed, and rounding cannot accumulate past one segment.
-//
+// without details.  Here the forward pass (the fast forward kernels, with
+// their record output on) writes per step the quantities the backward needs:
+// phi(k), u, the gates and a (about 1.3 KB per step and stream at d = 64).
+// This kernel starts from W_T and walks the steps backwards: each step
+// subtracts from W exactly the recorded rank-one update the forward added
+// (no matrix inversion, which would amplify rounding wherever the update
+// contracts W), so W_{t-1} is recovered to within a few ulps that grow like
+// sqrt(T).  x~ and dy are staged per KSEG-step segment, together with the
+// segment's records.
 // Layout: thread (rg = tid/4, cg = tid%4) holds rows rg + RG i (i < S) and the
 // D/4 columns of float4 chunks cg + 4 j.  Row dot products finish with two xor
 // shuffles over the four column groups; column sums over rows finish with a
@@ -44,12 +44,13 @@ namespace srwm {
 
 struct BwdParams {
     const float* x;        // [B, T, H, D]
-    const float* W0;       // [H, M, D]
+    const float* WT;       // [B, H, M, D]: W_T of every stream, from the forward pass
+    const float* rec;      // the forward's per-step records (KParams::emit layout)
+    int rec_stride;        // floats per record
     const float* dy;       // [B, T, H, D]
     const float* dWf;      // [B, H, M, D] or nullptr (zero)
     float* dx;             // [B, T, H, D]
     float* dW_seq;         // [B, H, M, D]: dL/dW0 of every stream (summed over b later)
-    float* snap;           // [B * H][n_seg - 1][M * D]: W at the start of segments 1..
     int B, T, H;
 };
 
@@ -186,59 +187,17 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
     };
     // x~ (and optionally dy) of steps t0 .. t0+len-1 into shared memory
     auto stage = [&](int t0, int len, bool with_dy) {
-        for (int idx = tid; idx < len * D; idx += C::NT) {
-            const int s = idx / D, c = idx - s * D;
+        constexpr int Q = D / 4;
+        for (int idx = tid; idx < len * Q; idx += C::NT) {
+            const int s = idx / Q, c = 4 * (idx - s * Q);
             const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D + c;
-            sm.xs[s][c] = bp.x[g];
-            if (with_dy) sm.dyv[s][c] = bp.dy[g];
+            *reinterpret_cast<float4*>(&sm.xs[s][c]) = __ldg(reinterpret_cast<const float4*>(bp.x + g));
+            if (with_dy) *reinterpret_cast<float4*>(&sm.dyv[s][c]) = __ldg(reinterpret_cast<const float4*>(bp.dy + g));
         }
         __syncthreads();
         if (softmax_input) {
             for (int s = warp; s < len; s += C::NW) warp_softmax<D>(sm.xs[s], sm.xs[s], lane);
             __syncthreads();
-        }
-    };
-    // one forward step (local index s) on the register tile, recording
-    // phi(k), u, gates and a
-    auto fwd_step = [&](int s) {
-        float zp[S];
-#pragma unroll
-        for (int i = 0; i < S; ++i) {
-            zp[i] = 0.f;
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) zp[i] = fmaf(w[i][q], sm.xs[s][bcol<C>(cg, q)], zp[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < S; ++i) {
-            zp[i] += __shfl_xor_sync(0xffffffffu, zp[i], 1);
-            zp[i] += __shfl_xor_sync(0xffffffffu, zp[i], 2);
-            if ((i & 3) == cg) sm.z[rg + RG * i] = zp[i];
-        }
-        __syncthreads();
-        if (warp == 0) {
-            warp_softmax<D>(sm.z + D, sm.pk[s], lane);
-            warp_softmax<D>(sm.z + 2 * D, sm.u[s], lane);   // phi(q) for now
-            if (lane < 4) sm.g[s][lane] = sigmoid_fast(sm.z[3 * D + (NLR == 4 ? lane : 0)]);
-            __syncwarp();
-            for (int c = lane; c < D; c += 32) sm.u[s][c] -= sm.pk[s][c];
-        }
-        __syncthreads();
-        float ap[S];
-#pragma unroll
-        for (int i = 0; i < S; ++i) {
-            ap[i] = 0.f;
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) ap[i] = fmaf(w[i][q], sm.u[s][bcol<C>(cg, q)], ap[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < S; ++i) {
-            ap[i] += __shfl_xor_sync(0xffffffffu, ap[i], 1);
-            ap[i] += __shfl_xor_sync(0xffffffffu, ap[i], 2);
-            const int r = rg + RG * i;
-            if ((i & 3) == cg) sm.a[s][r] = ap[i];
-            const float coef = sm.g[s][gidx(r)] * ap[i];
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) w[i][q] = fmaf(coef, sm.pk[s][bcol<C>(cg, q)], w[i][q]);
         }
     };
     // column sums over all rows of per-thread partials v[N] (N/CPT vectors):
@@ -263,18 +222,8 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
         __syncthreads();
     };
 
-    // ---- phase 1: states at the start of segments 1 .. nseg-1
-    load_state(bp.W0 + static_cast<size_t>(h) * MD);
-    for (int j = 0; j + 1 < nseg; ++j) {
-        stage(j * KSEG, KSEG, false);
-        for (int s = 0; s < KSEG; ++s) {
-            fwd_step(s);
-            __syncthreads();
-        }
-        store_tile(w, bp.snap + (static_cast<size_t>(p) * (nseg - 1) + j) * MD);
-    }
-
-    // ---- phase 2: segments backwards
+    // ---- W_T (from the forward pass) and dL/dW_T
+    load_state(bp.WT + static_cast<size_t>(p) * MD);
 #pragma unroll
     for (int i = 0; i < S; ++i) {
         const int r = rg + RG * i;
@@ -289,17 +238,53 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
             dw[i][4 * j + 3] = v.w;
         }
     }
-    __syncthreads();   // every thread is done writing the last snapshot
+    // ---- segments backwards; each step subtracts its recorded update from W
     for (int j = nseg - 1; j >= 0; --j) {
         const int t0 = j * KSEG;
         const int len = min(KSEG, T - t0);
-        if (j == 0) load_state(bp.W0 + static_cast<size_t>(h) * MD);
-        else load_state(bp.snap + (static_cast<size_t>(p) * (nseg - 1) + (j - 1)) * MD);
         stage(t0, len, true);
-        for (int s = 0; s < len; ++s) {
-            fwd_step(s);
-            __syncthreads();
+        // the forward's records of the segment: phi(k), u, gates, a.  float4
+        // pieces (every field starts at a multiple of 4 floats), four loads in
+        // flight per thread; a record's tail past row M-1 and the padded rows
+        // up to MP are zeroed.
+        {
+            const int q4 = bp.rec_stride >> 2;   // float4 per record
+            const float4* src = reinterpret_cast<const float4*>(bp.rec + (static_cast<size_t>(p) * T + t0) * bp.rec_stride);
+            const int n4 = len * q4;
+            for (int base = tid; base < n4; base += 4 * C::NT) {
+                float4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int q = base + k * C::NT;
+                    if (q < n4) v[k] = __ldg(src + q);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int q = base + k * C::NT;
+                    if (q >= n4) continue;
+                    const int s = q / q4, e = 4 * (q - s * q4);
+                    if (e < D) {
+                        *reinterpret_cast<float4*>(&sm.pk[s][e]) = v[k];
+                    } else if (e < 2 * D) {
+                        *reinterpret_cast<float4*>(&sm.u[s][e - D]) = v[k];
+                    } else if (e < 2 * D + 4) {
+                        *reinterpret_cast<float4*>(&sm.g[s][0]) = v[k];
+                    } else {
+                        const int r = e - 2 * D - 4;
+                        sm.a[s][r + 0] = r + 0 < M ? v[k].x : 0.f;
+                        sm.a[s][r + 1] = r + 1 < M ? v[k].y : 0.f;
+                        sm.a[s][r + 2] = r + 2 < M ? v[k].z : 0.f;
+                        sm.a[s][r + 3] = r + 3 < M ? v[k].w : 0.f;
+                    }
+                }
+            }
+            constexpr int R0 = (emit_record_floats(D, NLR) - 2 * D - 4);   // rows covered by a record
+            for (int idx = tid; idx < len * (C::MP - R0); idx += C::NT) {
+                const int s = idx / (C::MP - R0);
+                sm.a[s][R0 + idx - s * (C::MP - R0)] = 0.f;
+            }
         }
+        __syncthreads();
         for (int s = len - 1; s >= 0; --s) {
             // 1. step back: W_{t-1} = W_t - coef (outer) pk; dcoef = dW pk
             float av[S], dco[S];

@@ -35,7 +35,15 @@ struct KParams {
     // segments; NULL otherwise).  Segment s of a stream waits until its count
     // reaches s; its state comes from W_out, where segment s - 1 left it.
     int* seg_done;
+    // Per-step records for the backward pass (NULL: none).  Record of stream p,
+    // step t (of the whole sequence) at emit + (p * T + t) * emit_stride:
+    //   [phi(k_t) (d) | u_t = phi(q_t) - phi(k_t) (d) | gates (4) | a_t = W_{t-1} u_t (m)]
+    float* emit;
+    int emit_stride;   // floats per record, a multiple of 4
 };
+
+// Floats per backward record (see KParams::emit), rounded up to 16 bytes.
+SRWM_HD constexpr int emit_record_floats(int d, int n_lr) { return (2 * d + 4 + 3 * d + n_lr + 3) / 4 * 4; }
 
 // What the host needs to launch one template instantiation.
 struct LaunchInfo {
@@ -46,8 +54,9 @@ struct LaunchInfo {
     int tau;              // steps per TMA chunk (box height of the x / y tensor maps)
 };
 
-LaunchInfo launch_info_d16(int n_lr, int softmax_input);
-LaunchInfo launch_info_d32(int n_lr, int softmax_input);
-LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm);
+// emit: the instantiation that also writes the backward records (KParams::emit).
+LaunchInfo launch_info_d16(int n_lr, int softmax_input, bool emit = false);
+LaunchInfo launch_info_d32(int n_lr, int softmax_input, bool emit = false);
+LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm, bool emit = false);
 
 }  // namespace srwm

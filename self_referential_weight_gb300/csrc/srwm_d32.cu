@@ -4,8 +4,12 @@
 
 namespace srwm {
 
-LaunchInfo launch_info_d32(int n_lr, int softmax_input)
+LaunchInfo launch_info_d32(int n_lr, int softmax_input, bool emit)
 {
+    if (emit) {
+        if (n_lr == 1) return softmax_input ? launch_info<32, 1, true, true>() : launch_info<32, 1, false, true>();
+        return softmax_input ? launch_info<32, 4, true, true>() : launch_info<32, 4, false, true>();
+    }
     if (n_lr == 1) return softmax_input ? launch_info<32, 1, true>() : launch_info<32, 1, false>();
     return softmax_input ? launch_info<32, 4, true>() : launch_info<32, 4, false>();
 }

@@ -5,6 +5,25 @@
 
 namespace srwm {
 
+namespace {
+
+template <bool EMIT>
+LaunchInfo pick(int n_lr, int softmax_input, bool two_warps)
+{
+    if constexpr (!EMIT) {
+        if (two_warps) {
+            if (n_lr == 1)
+                return softmax_input ? launch_info_d64w2_impl<1, true>() : launch_info_d64w2_impl<1, false>();
+            return softmax_input ? launch_info_d64w2_impl<4, true>() : launch_info_d64w2_impl<4, false>();
+        }
+    }
+    if (n_lr == 1)
+        return softmax_input ? launch_info_d64_impl<4, 1, true, EMIT>() : launch_info_d64_impl<4, 1, false, EMIT>();
+    return softmax_input ? launch_info_d64_impl<4, 4, true, EMIT>() : launch_info_d64_impl<4, 4, false, EMIT>();
+}
+
+}  // namespace
+
 // Two kernels, chosen by the number of (sequence, head) streams per SM:
 //   * up to two per SM: four warps per stream (two CTAs per SM).  Each stream
 //     then has a slot of its own, and four warps give the shortest step.
@@ -13,14 +32,13 @@ namespace srwm {
 //     and that traffic grows with the warp count.)
 //   * more: two warps per stream, four CTAs per SM, so twice as many streams
 //     advance at once.
-LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm)
+// emit selects the instantiations that also write the backward records: the
+// four-warp kernel at any stream count (the two-warp kernel has no registers
+// to spare for the record stores).
+LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm, bool emit)
 {
-    if (n_streams > 2LL * n_sm) {
-        if (n_lr == 1) return softmax_input ? launch_info_d64w2_impl<1, true>() : launch_info_d64w2_impl<1, false>();
-        return softmax_input ? launch_info_d64w2_impl<4, true>() : launch_info_d64w2_impl<4, false>();
-    }
-    if (n_lr == 1) return softmax_input ? launch_info_d64_impl<4, 1, true>() : launch_info_d64_impl<4, 1, false>();
-    return softmax_input ? launch_info_d64_impl<4, 4, true>() : launch_info_d64_impl<4, 4, false>();
+    const bool two_warps = n_streams > 2LL * n_sm;
+    return emit ? pick<true>(n_lr, softmax_input, two_warps) : pick<false>(n_lr, softmax_input, two_warps);
 }
 
 }  // namespace srwm

@@ -95,11 +95,11 @@ __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&o
 // inputs and x~_{t+1} from shared memory, applies the pending update, writes
 // z_{t+1} (y rows to the staging buffer) and leaves this step's update pending
 // in (coef, pkc).
-template <int NW, int NS, int NLR>
+template <int NW, int NS, int NLR, bool EMIT = false>
 __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int lane, int warp, int rg, int cg,
                                          float2 (&w)[d64::Cfg<NW>::SLOTS + 1][d64::NP],
                                          float (&coef)[d64::Cfg<NW>::SLOTS + 1], float2 (&pkc)[d64::NP],
-                                         const float* xn)
+                                         const float* xn, float* em = nullptr)
 {
     using namespace d64;
     using C = Cfg<NW>;
@@ -146,6 +146,16 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
     pkq[lane + 32] = pk1;
     pkq[D + lane] = pq0;
     pkq[D + lane + 32] = pq1;
+    if constexpr (EMIT) {
+        // backward record: phi(k), u, gates (u as the column pass forms it: pq - pk)
+        if (warp == 0) {
+            em[lane] = pk0;
+            em[lane + 32] = pk1;
+            em[D + lane] = pq0 - pk0;
+            em[D + lane + 32] = pq1 - pk1;
+            if (lane < 4) em[2 * D + lane] = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3];
+        }
+    }
     __syncwarp();
     float2 u2[NP];
     {
@@ -191,6 +201,12 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
         const int blk = (NLR == 1) ? 0 : (i < SLOTS ? C::block_of_slot(i) : 3);
         coef[i] = g[blk] * a[i];
         const float zr = fmaf(coef[i], s, bb[i]);
+        if constexpr (EMIT) {
+            if ((i & 3) == cg) {
+                if (i < SLOTS) em[2 * D + 4 + rg + RG * i] = a[i];
+                else if (3 * D + rg < M) em[2 * D + 4 + 3 * D + rg] = a[i];
+            }
+        }
         if ((i & 3) == cg) {
             if (i < SLOTS && C::block_of_slot(i) == 0) {
                 if (write_y) yrow[rg + RG * i] = zr;
@@ -204,7 +220,7 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
     if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
 }
 
-template <int NW, int NLR, bool SMX>
+template <int NW, int NLR, bool SMX, bool EMIT = false>
 __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     srwm_d64_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                     const KParams kp)
@@ -358,8 +374,10 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
         // Warp 0 also carries the beta rows; a compile-time slot count keeps
         // each role's step free of branches.
         auto step = [&](int t, const float* xn) {
-            if (has_beta) d64_step<NW, S1, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn);
-            else d64_step<NW, SLOTS, NLR>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn);
+            float* em = nullptr;
+            if constexpr (EMIT) em = kp.emit + (static_cast<size_t>(p) * kp.T + t0 + t) * kp.emit_stride;
+            if (has_beta) d64_step<NW, S1, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn, em);
+            else d64_step<NW, SLOTS, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn, em);
         };
         if constexpr (!SMX) {
             // x~ = x is read straight from the ring, chunk by chunk: the inner
@@ -476,10 +494,10 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     }
 }
 
-template <int NW, int NLR, bool SMX>
+template <int NW, int NLR, bool SMX, bool EMIT = false>
 LaunchInfo launch_info_d64_impl()
 {
-    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64_kernel<NW, NLR, SMX>), d64::Cfg<NW>::NT, 1,
+    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64_kernel<NW, NLR, SMX, EMIT>), d64::Cfg<NW>::NT, 1,
                       static_cast<int>(sizeof(d64::Smem<NW>)) + 128, d64::TAU};
 }
 

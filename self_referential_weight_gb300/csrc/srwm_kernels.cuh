@@ -83,7 +83,7 @@ struct __align__(128) WarpSmem {
     uint64_t xbar[2];               // "chunk landed" barriers of the x ring
 };
 
-template <int D, int NLR, bool SMX>
+template <int D, int NLR, bool SMX, bool EMIT = false>
 __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
     srwm_warp_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const KParams kp)
@@ -243,6 +243,16 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
                 sm.pk[col] = pk;
                 sm.pq[col] = pq;
             }
+            // backward record of step t: phi(k), u = pq - pk, gates (a follows below)
+            float* em = nullptr;
+            if constexpr (EMIT) {
+                em = kp.emit + (static_cast<size_t>(p) * kp.T + t0 + t) * kp.emit_stride;
+                if (lane < D) {
+                    em[col] = pk;
+                    em[D + col] = pq - pk;
+                }
+                if (lane < 4) em[2 * D + lane] = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3];
+            }
             {
                 const int tn = t + 2;
                 bool ok = true;
@@ -316,6 +326,9 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
                         w[i][4 * j + 3] = fmaf(coef, pkv[j].w, w[i][4 * j + 3]);
                     }
                     const float zr = fmaf(coef, s, bb[i]);
+                    if constexpr (EMIT) {
+                        if ((i & 3) == cg && rg + 8 * i < C::M) em[2 * D + 4 + rg + 8 * i] = a[i];
+                    }
                     if ((i & 3) == cg) {
                         const int r = rg + 8 * i;
                         if (r < D) {
@@ -374,11 +387,11 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
     }
 }
 
-template <int D, int NLR, bool SMX>
+template <int D, int NLR, bool SMX, bool EMIT = false>
 LaunchInfo launch_info()
 {
     using C = WarpCfg<D, NLR, SMX>;
-    return LaunchInfo{reinterpret_cast<const void*>(&srwm_warp_kernel<D, NLR, SMX>), C::NT, C::PPC,
+    return LaunchInfo{reinterpret_cast<const void*>(&srwm_warp_kernel<D, NLR, SMX, EMIT>), C::NT, C::PPC,
                       static_cast<int>(C::PPC * sizeof(WarpSmem<C>)) + 128, C::TAU};
 }
 

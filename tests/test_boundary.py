@@ -154,12 +154,17 @@ def test_backward_workspace_bytes(lib):
     SZ, I = ctypes.c_size_t, ctypes.c_int
     L.srwm_backward_workspace_bytes.argtypes = [I, I, I, I, I]
     L.srwm_backward_workspace_bytes.restype = SZ
-    # 4 bytes * B * H * m * d * ceil(T / 32), rounded up to 256
-    for B, T, H, d, n_lr in [(2, 75, 3, 16, 4), (1, 32, 1, 64, 1), (5, 1, 2, 32, 4), (64, 1024, 8, 64, 4)]:
+    # regions, each rounded up to 256 bytes: dL/dW0 per stream and W_T
+    # (B*H*m*d floats each), the forward's y (B*T*H*d), the per-step records
+    # (B*H*T records of ceil4(5d + 4 + n_lr) floats), the counters (B*H ints)
+    def expect(B, T, H, d, n_lr):
+        a = lambda n: (n + 255) // 256 * 256
         m = 3 * d + n_lr
-        raw = 4 * B * H * m * d * ((T + 31) // 32)
-        assert L.srwm_backward_workspace_bytes(B, T, H, d, n_lr) == (raw + 255) // 256 * 256
-    assert L.srwm_backward_workspace_bytes(2, 0, 3, 16, 4) == (4 * 2 * 3 * 52 * 16 + 255) // 256 * 256
+        rec = (5 * d + 4 + n_lr + 3) // 4 * 4
+        return 2 * a(4 * B * H * m * d) + a(4 * B * T * H * d) + a(4 * B * H * T * rec) + a(4 * B * H)
+    for B, T, H, d, n_lr in [(2, 75, 3, 16, 4), (1, 32, 1, 64, 1), (5, 1, 2, 32, 4), (64, 1024, 8, 64, 4)]:
+        assert L.srwm_backward_workspace_bytes(B, T, H, d, n_lr) == expect(B, T, H, d, n_lr)
+    assert L.srwm_backward_workspace_bytes(2, 0, 3, 16, 4) == expect(2, 0, 3, 16, 4)
     assert L.srwm_backward_workspace_bytes(2, 5, 3, 48, 4) == 0
     assert L.srwm_backward_workspace_bytes(2, 5, 3, 16, 2) == 0
     assert L.srwm_backward_workspace_bytes(0, 5, 3, 16, 4) == 0
