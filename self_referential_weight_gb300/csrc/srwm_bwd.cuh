@@ -83,6 +83,8 @@ struct __align__(16) BwdSmem {
     float dgrow[C::MP];
     float red[C::NW][2][C::D];   // per-warp column partials
     float vec[2][C::D];          // column sums
+    float bred[C::NW][4];        // per-warp block sums of dcoef a
+    float bsum[4];               // their sums over warps
 };
 
 template <class C>
@@ -222,6 +224,50 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
         __syncthreads();
     };
 
+    // colsum with two vectors, plus four block sums (bs: per-thread partials):
+    // afterwards sm.vec[0..1] hold the column sums and sm.bsum[0..3] the
+    // block sums, all in a fixed order of warps (deterministic)
+    auto colsum_gate = [&](float (&v)[C::NV2], float (&bsum4)[4]) {
+        constexpr int N = C::NV2;
+        rowgroup_reduce<N>(v, lane);
+        const int rg_lo = (lane >> 2) & 7;
+#pragma unroll
+        for (int e = 0; e < N / 8; ++e) {
+            const int idx = rg_lo * (N / 8) + e;
+            const int vv = idx / CPT, q = idx - vv * CPT;
+            sm.red[warp][vv][bcol<C>(cg, q)] = v[e];
+        }
+        // the block sums over the warp's 32 lanes: two transposed levels,
+        // then three plain ones; lane bits (4, 3) select the block
+        {
+            const bool hi16 = (lane & 16) != 0;
+            float k0 = hi16 ? bsum4[2] : bsum4[0], k1 = hi16 ? bsum4[3] : bsum4[1];
+            const float s0 = hi16 ? bsum4[0] : bsum4[2], s1 = hi16 ? bsum4[1] : bsum4[3];
+            k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+            k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+            const bool hi8 = (lane & 8) != 0;
+            float k = hi8 ? k1 : k0;
+            k += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+            k += __shfl_xor_sync(0xffffffffu, k, 4);
+            k += __shfl_xor_sync(0xffffffffu, k, 2);
+            k += __shfl_xor_sync(0xffffffffu, k, 1);
+            if ((lane & 7) == 0) sm.bred[warp][lane >> 3] = k;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 2 * D + 4; idx += C::NT) {
+            float acc = 0.f;
+            if (idx < 2 * D) {
+                const int vv = idx / D, c = idx - vv * D;
+                for (int ww = 0; ww < C::NW; ++ww) acc += sm.red[ww][vv][c];
+                sm.vec[vv][c] = acc;
+            } else {
+                for (int ww = 0; ww < C::NW; ++ww) acc += sm.bred[ww][idx - 2 * D];
+                sm.bsum[idx - 2 * D] = acc;
+            }
+        }
+        __syncthreads();
+    };
+
     // ---- W_T (from the forward pass) and dL/dW_T
     load_state(bp.WT + static_cast<size_t>(p) * MD);
 #pragma unroll
@@ -306,78 +352,87 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
                 dco[i] += __shfl_xor_sync(0xffffffffu, dco[i], 1);
                 dco[i] += __shfl_xor_sync(0xffffffffu, dco[i], 2);
             }
-            // 2. column sums: v1 = dW'^T coef, v2 = W^T da
+            // 2. column sums v1 = dW'^T coef, v2 = W^T da, and the gate
+            // gradients' block sums of dcoef a (slot i is block i here)
             float da[S];
             float cv[C::NV2];
 #pragma unroll
             for (int q = 0; q < C::NV2; ++q) cv[q] = 0.f;
+            float bs[4];
 #pragma unroll
             for (int i = 0; i < S; ++i) {
                 const int r = rg + RG * i;
                 const float g = sm.g[s][gidx(r)];
                 const float coef = g * av[i];
                 da[i] = g * dco[i];
-                if ((i & 3) == cg) sm.dgrow[r] = dco[i] * av[i];
+                bs[i] = cg == 0 ? dco[i] * av[i] : 0.f;
 #pragma unroll
                 for (int q = 0; q < CPT; ++q) {
                     cv[q] = fmaf(dw[i][q], coef, cv[q]);
                     cv[CPT + q] = fmaf(w[i][q], da[i], cv[CPT + q]);
                 }
             }
-            colsum(cv, 2);   // sm.vec[0] = v1, sm.vec[1] = v2 (dgrow visible too)
-            // 3. softmax backward and dbeta (warp 0) -> dz
-            if (warp == 0) {
-                float* dpk = sm.vec[0];
-                float* dpq = sm.vec[1];
-                for (int c = lane; c < D; c += 32) dpk[c] -= dpq[c];   // v1 - v2
-                __syncwarp();
-                float* pq = sm.z;   // scratch: pq = u + pk
-                for (int c = lane; c < D; c += 32) pq[c] = sm.u[s][c] + sm.pk[s][c];
-                __syncwarp();
-                warp_softmax_bwd<D>(sm.pk[s], dpk, sm.dz + D, lane);
-                warp_softmax_bwd<D>(pq, dpq, sm.dz + 2 * D, lane);
-                for (int c = lane; c < D; c += 32) sm.dz[c] = sm.dyv[s][c];
-                // dbeta per block: sum of dcoef a over the block's rows
-                float part[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int r = lane; r < M; r += 32) part[blk(r)] += sm.dgrow[r];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) part[k] = group_sum<32>(part[k]);
-                if (lane < NLR) {
-                    const float g = sm.g[s][lane];
-                    sm.dz[3 * D + lane] = part[lane] * g * (1.f - g);
-                }
-                for (int r = M + lane; r < C::MP; r += 32) sm.dz[r] = 0.f;
+            if constexpr (NLR == 1) {
+                bs[0] = (bs[0] + bs[1]) + (bs[2] + bs[3]);
+                bs[1] = bs[2] = bs[3] = 0.f;
             }
-            __syncthreads();
+            colsum_gate(cv, bs);   // sm.vec[0] = v1, sm.vec[1] = v2, sm.bsum[j] = block j's sum
+            // 3. dz for this thread's rows: y row dy; k, q rows through the
+            // softmax backward; beta row through the sigmoid
+            float dz[S];
+            {
+                const float* v1 = sm.vec[0];
+                const float* v2 = sm.vec[1];
+                float dk = 0.f, dq = 0.f;   // <phi(k), dphi(k)>, <phi(q), dphi(q)>
+                for (int c = lane; c < D; c += 32) {
+                    const float pkc = sm.pk[s][c], pqc = sm.u[s][c] + pkc;
+                    dk = fmaf(pkc, v1[c] - v2[c], dk);
+                    dq = fmaf(pqc, v2[c], dq);
+                }
+                dk = group_sum<32>(dk);
+                dq = group_sum<32>(dq);
+                const float pkr = sm.pk[s][rg], pqr = sm.u[s][rg] + pkr;
+                dz[0] = sm.dyv[s][rg];
+                dz[1] = pkr * ((v1[rg] - v2[rg]) - dk);
+                dz[2] = pqr * (v2[rg] - dq);
+                dz[3] = 0.f;
+                if (rg < NLR) {
+                    const float g = sm.g[s][rg];
+                    dz[3] = sm.bsum[rg] * g * (1.f - g);
+                }
+            }
             // 4. dW += da (outer) u + dz (outer) x~ ; column partials of W^T dz
             float cx[C::NV1];
 #pragma unroll
             for (int q = 0; q < C::NV1; ++q) cx[q] = 0.f;
 #pragma unroll
             for (int i = 0; i < S; ++i) {
-                const float dzr = sm.dz[rg + RG * i];
 #pragma unroll
                 for (int q = 0; q < CPT; ++q) {
                     const int c = bcol<C>(cg, q);
                     dw[i][q] = fmaf(da[i], sm.u[s][c], dw[i][q]);
-                    dw[i][q] = fmaf(dzr, sm.xs[s][c], dw[i][q]);
-                    cx[q] = fmaf(w[i][q], dzr, cx[q]);
+                    dw[i][q] = fmaf(dz[i], sm.xs[s][c], dw[i][q]);
+                    cx[q] = fmaf(w[i][q], dz[i], cx[q]);
                 }
             }
             colsum(cx, 1);   // sm.vec[0] = dx~
-            // 5. dx (through the input softmax when present)
-            if (warp == 0) {
-                float* dxv = sm.vec[0];
-                if (softmax_input) {
-                    warp_softmax_bwd<D>(sm.xs[s], dxv, sm.vec[1], lane);
-                    __syncwarp();
-                    dxv = sm.vec[1];
+            // 5. dx (through the input softmax when present).  No barrier
+            // follows: sm.vec and sm.red are next written after the next
+            // column sum's first barrier, which these readers reach first.
+            const size_t gx = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
+            if (softmax_input) {
+                if (warp == 0) {
+                    const float* dxv = sm.vec[0];
+                    float dot = 0.f;
+                    for (int c = lane; c < D; c += 32) dot = fmaf(sm.xs[s][c], dxv[c], dot);
+                    dot = group_sum<32>(dot);
+                    for (int c = lane; c < D; c += 32) bp.dx[gx + c] = sm.xs[s][c] * (dxv[c] - dot);
                 }
-                const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
-                for (int c = lane; c < D; c += 32) bp.dx[g + c] = dxv[c];
+            } else if (tid < D) {
+                bp.dx[gx + tid] = sm.vec[0][tid];
             }
-            __syncthreads();
         }
+        __syncthreads();   // the segment's staged vectors are read before the next segment's staging
     }
     store_tile(dw, bp.dW_seq + static_cast<size_t>(p) * MD);
 }
