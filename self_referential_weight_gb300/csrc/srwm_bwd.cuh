@@ -159,7 +159,10 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
     auto blk = [](int r) { return NLR == 1 ? 0 : (r < 3 * D ? r / D : 3); };
     auto gidx = [&](int r) { return blk(r); };
 
-    float w[S][CPT], dw[S][CPT];
+    // W and dL/dW as pairs of adjacent columns (2q, 2q+1 of the thread's
+    // columns) for the two-wide FMA
+    constexpr int CP = CPT / 2;
+    float2 w[S][CP], dw[S][CP];
 
     auto load_state = [&](const float* src) {
 #pragma unroll
@@ -169,14 +172,12 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
             for (int j = 0; j < C::NCH; ++j) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (r < M) v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
-                w[i][4 * j + 0] = v.x;
-                w[i][4 * j + 1] = v.y;
-                w[i][4 * j + 2] = v.z;
-                w[i][4 * j + 3] = v.w;
+                w[i][2 * j] = make_float2(v.x, v.y);
+                w[i][2 * j + 1] = make_float2(v.z, v.w);
             }
         }
     };
-    auto store_tile = [&](float (&m)[S][CPT], float* dst) {
+    auto store_tile = [&](float2 (&m)[S][CP], float* dst) {
 #pragma unroll
         for (int i = 0; i < S; ++i) {
             const int r = rg + RG * i;
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
 #pragma unroll
             for (int j = 0; j < C::NCH; ++j)
                 *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
-                    make_float4(m[i][4 * j + 0], m[i][4 * j + 1], m[i][4 * j + 2], m[i][4 * j + 3]);
+                    make_float4(m[i][2 * j].x, m[i][2 * j].y, m[i][2 * j + 1].x, m[i][2 * j + 1].y);
         }
     };
     // x~ (and optionally dy) of steps t0 .. t0+len-1 into shared memory
@@ -278,10 +279,8 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (bp.dWf != nullptr && r < M)
                 v = *reinterpret_cast<const float4*>(bp.dWf + static_cast<size_t>(p) * MD + static_cast<size_t>(r) * D + 4 * (cg + 4 * j));
-            dw[i][4 * j + 0] = v.x;
-            dw[i][4 * j + 1] = v.y;
-            dw[i][4 * j + 2] = v.z;
-            dw[i][4 * j + 3] = v.w;
+            dw[i][2 * j] = make_float2(v.x, v.y);
+            dw[i][2 * j + 1] = make_float2(v.z, v.w);
         }
     }
     // ---- segments backwards; each step subtracts its recorded update from W
@@ -339,13 +338,15 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
                 const int r = rg + RG * i;
                 av[i] = sm.a[s][r];
                 const float coef = sm.g[s][gidx(r)] * av[i];
-                dco[i] = 0.f;
+                const float2 nc = make_float2(-coef, -coef);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < CPT; ++q) {
-                    const float pkc = sm.pk[s][bcol<C>(cg, q)];
-                    w[i][q] = fmaf(-coef, pkc, w[i][q]);
-                    dco[i] = fmaf(dw[i][q], pkc, dco[i]);
+                for (int q = 0; q < CP; ++q) {
+                    const float2 pk2 = *reinterpret_cast<const float2*>(&sm.pk[s][bcol<C>(cg, 2 * q)]);
+                    w[i][q] = __ffma2_rn(nc, pk2, w[i][q]);
+                    acc = __ffma2_rn(dw[i][q], pk2, acc);
                 }
+                dco[i] = acc.x + acc.y;
             }
 #pragma unroll
             for (int i = 0; i < S; ++i) {
@@ -356,20 +357,31 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
             // gradients' block sums of dcoef a (slot i is block i here)
             float da[S];
             float cv[C::NV2];
-#pragma unroll
-            for (int q = 0; q < C::NV2; ++q) cv[q] = 0.f;
             float bs[4];
+            {
+                float2 c1[CP], c2[CP];
 #pragma unroll
-            for (int i = 0; i < S; ++i) {
-                const int r = rg + RG * i;
-                const float g = sm.g[s][gidx(r)];
-                const float coef = g * av[i];
-                da[i] = g * dco[i];
-                bs[i] = cg == 0 ? dco[i] * av[i] : 0.f;
+                for (int q = 0; q < CP; ++q) c1[q] = c2[q] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < CPT; ++q) {
-                    cv[q] = fmaf(dw[i][q], coef, cv[q]);
-                    cv[CPT + q] = fmaf(w[i][q], da[i], cv[CPT + q]);
+                for (int i = 0; i < S; ++i) {
+                    const int r = rg + RG * i;
+                    const float g = sm.g[s][gidx(r)];
+                    const float coef = g * av[i];
+                    da[i] = g * dco[i];
+                    bs[i] = cg == 0 ? dco[i] * av[i] : 0.f;
+                    const float2 cc = make_float2(coef, coef), dd = make_float2(da[i], da[i]);
+#pragma unroll
+                    for (int q = 0; q < CP; ++q) {
+                        c1[q] = __ffma2_rn(dw[i][q], cc, c1[q]);
+                        c2[q] = __ffma2_rn(w[i][q], dd, c2[q]);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < CP; ++q) {
+                    cv[2 * q] = c1[q].x;
+                    cv[2 * q + 1] = c1[q].y;
+                    cv[CPT + 2 * q] = c2[q].x;
+                    cv[CPT + 2 * q + 1] = c2[q].y;
                 }
             }
             if constexpr (NLR == 1) {
@@ -403,16 +415,27 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
             }
             // 4. dW += da (outer) u + dz (outer) x~ ; column partials of W^T dz
             float cx[C::NV1];
+            {
+                float2 c3[CP];
 #pragma unroll
-            for (int q = 0; q < C::NV1; ++q) cx[q] = 0.f;
+                for (int q = 0; q < CP; ++q) c3[q] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < S; ++i) {
+                for (int i = 0; i < S; ++i) {
+                    const float2 dd = make_float2(da[i], da[i]), zz = make_float2(dz[i], dz[i]);
 #pragma unroll
-                for (int q = 0; q < CPT; ++q) {
-                    const int c = bcol<C>(cg, q);
-                    dw[i][q] = fmaf(da[i], sm.u[s][c], dw[i][q]);
-                    dw[i][q] = fmaf(dz[i], sm.xs[s][c], dw[i][q]);
-                    cx[q] = fmaf(w[i][q], dz[i], cx[q]);
+                    for (int q = 0; q < CP; ++q) {
+                        const int c = bcol<C>(cg, 2 * q);
+                        dw[i][q] = __ffma2_rn(dd, *reinterpret_cast<const float2*>(&sm.u[s][c]), dw[i][q]);
+                        dw[i][q] = __ffma2_rn(zz, *reinterpret_cast<const float2*>(&sm.xs[s][c]), dw[i][q]);
+                        c3[q] = __ffma2_rn(w[i][q], zz, c3[q]);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < C::NV1; ++q) cx[q] = 0.f;
+#pragma unroll
+                for (int q = 0; q < CP; ++q) {
+                    cx[2 * q] = c3[q].x;
+                    cx[2 * q + 1] = c3[q].y;
                 }
             }
             colsum(cx, 1);   // sm.vec[0] = dx~
