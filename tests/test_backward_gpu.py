@@ -104,3 +104,19 @@ def test_backward_small_workspace_rejected():
     with pytest.raises(binding.SrwmError) as e:
         binding.srwm_backward(t(x), t(W0), 4, False, t(dy), workspace=ws)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("name,h", [("mid", 5), ("rl", 2)])
+def test_backward_full_size_sampled_head(name, h):
+    """Full-size workload through srwm_backward (the launch a training step
+    makes); the oracle recomputes one head over every sequence: that head's
+    dL/dx and dL/dW0[h] (heads are independent, so the slice's gradients are
+    the full problem's)."""
+    wl = inputs.workload(name)
+    x, W0 = inputs.make_inputs(wl)
+    dy, _ = inputs.make_cotangents(wl, False)
+    dx, dW0 = run_bwd(x, W0, wl.n_lr, wl.softmax_input, dy, None)
+    xs = np.ascontiguousarray(x[:, :, h:h + 1])
+    ox, oW = srwm_grad.grads(xs, W0[h:h + 1], wl.n_lr, wl.softmax_input, np.ascontiguousarray(dy[:, :, h:h + 1]))
+    assert rel(dx[:, :, h:h + 1], ox) <= TOL, rel(dx[:, :, h:h + 1], ox)
+    assert rel(dW0[h:h + 1], oW) <= TOL, rel(dW0[h:h + 1], oW)
