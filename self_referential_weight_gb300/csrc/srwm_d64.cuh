@@ -151,8 +151,8 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
         if (warp == 0) {
             em[lane] = pk0;
             em[lane + 32] = pk1;
-            em[D + lane] = pq0 - pk0;
-            em[D + lane + 32] = pq1 - pk1;
+            em[D + lane] = __fsub_rn(pq0, pk0);   // as the column pass forms it (no contraction)
+            em[D + lane + 32] = __fsub_rn(pq1, pk1);
             if (lane < 4) em[2 * D + lane] = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3];
         }
     }

@@ -134,8 +134,11 @@ __device__ __forceinline__ void d64w2_step(d64w2::Smem& sm, int t, int T, int la
     // ---- 2. phi_k, u -> the warp's buffer; s = phi_k . x~_{t+1}
     pk_cur[lane] = pk0;
     pk_cur[lane + 32] = pk1;
-    u_cur[lane] = pq0 - pk0;
-    u_cur[lane + 32] = pq1 - pk1;
+    // u = phi(q) - phi(k) with an explicit rounded subtraction: a contracted
+    // fma(e_q, 1/sum_q, -phi(k)) would skip phi(q)'s rounding, so equal k and
+    // q rows would no longer give u = 0 exactly
+    u_cur[lane] = __fsub_rn(pq0, pk0);
+    u_cur[lane + 32] = __fsub_rn(pq1, pk1);
     const float s = warp_allsum(fmaf(pk0, xn[lane], pk1 * xn[lane + 32]));
     __syncwarp();
 

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(WarpCfg<D, NLR, SMX>::NT, 2)
                 em = kp.emit + (static_cast<size_t>(p) * kp.T + t0 + t) * kp.emit_stride;
                 if (lane < D) {
                     em[col] = pk;
-                    em[D + col] = pq - pk;
+                    em[D + col] = __fsub_rn(pq, pk);   // as the row pass forms it (no contraction)
                 }
                 if (lane < 4) em[2 * D + lane] = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3];
             }
