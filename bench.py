@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time srwm_backward (gradients of a loss on y) on the workload instead; prints its own line")
     ap.add_argument("--layer", action="store_true",
                     help="time one Recursive Self-Transformer layer (SRWM + LN + FF + residual, d_ff = 4D) "
                          "on the workload's shape instead; prints its own line")
@@ -258,6 +260,8 @@ def main():
 
     if args.layer:
         return bench_layer(args, wl)
+    if args.backward:
+        return bench_backward(args, wl)
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, wl)
@@ -458,6 +462,55 @@ def fma_probe(binding, n_sm, stream):
         fmas = blocks * threads * iters * 8 * (2 if packed else 1)
         res["tflops_packed" if packed else "tflops_scalar"] = 2 * fmas / s / 1e12
     return res
+
+
+def bench_backward(args, wl):
+    """srwm_backward on the workload: dL/dx and dL/dW0 of L = <dy, y> (1 GPU,
+    L2 flushed between timed calls).  One call runs the forward with its
+    per-step records, then the steps backwards; its arithmetic is 3md (forward)
+    + 7md (backward step) FMAs per head-token."""
+    import torch
+    from self_referential_weight_gb300 import binding
+
+    dev = torch.device("cuda:0")
+    x_np, W0_np = inputs.make_inputs(wl)
+    dy_np, _ = inputs.make_cotangents(wl, False)
+    x, W0, dy = (torch.from_numpy(a).to(dev) for a in (x_np, W0_np, dy_np))
+    dx, dW0 = torch.empty_like(x), torch.empty_like(W0)
+    ws = torch.empty(binding.srwm_backward_workspace_bytes(wl.B, wl.T, wl.H, wl.d, wl.n_lr), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        binding.srwm_backward(x, W0, wl.n_lr, wl.softmax_input, dy, None, dx, dW0, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    if binding.srwm_last_device_status() != 0:
+        raise RuntimeError("device status set")
+    t = statistics.median(ts)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = n_sm * FMA_PER_CLK_PER_SM * 2 * 2070e6 / 1e12
+    flops = 2 * 10 * wl.m * wl.d * wl.head_tokens
+    print(json.dumps({
+        "metric": "SRWM backward (dL/dx, dL/dW0), head-token gradients/s (1 GB300)",
+        "value": wl.head_tokens / (t / 1e3), "unit": "head-token gradients/s", "ms_per_step": t, "steps": steps,
+        "config": workload_config(wl), "dtype": "f32", "data": "synthetic",
+        "fp32_fma_frac": flops / (t / 1e3) / 1e12 / peak,
+        "fma_basis": "3md forward + 7md backward FMAs per head-token; 2070 MHz peak",
+        "workspace_bytes": ws.numel(),
+    }), flush=True)
 
 
 def bench_layer(args, wl):
