@@ -41,6 +41,7 @@ L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
 KERNEL_SOURCES = {
     "srwm_d64_kernel": ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
     "srwm_d64w2_kernel": ["srwm_d64w2.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
+    "srwm_d32_kernel": ["srwm_d32.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d32.cu"],
     "srwm_warp_kernel": ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h"],
 }
 
@@ -93,9 +94,12 @@ def fmas_per_head_token(wl):
 
 
 def kernel_name(wl, n_sm):
-    """The kernel the library launches for this workload (see srwm_d64.cu)."""
-    if wl.d != 64:
+    """The kernel the library launches for this workload (see srwm_d32.cu and
+    srwm_d64.cu)."""
+    if wl.d == 16:
         return "srwm_warp_kernel"
+    if wl.d == 32:
+        return "srwm_d32_kernel"
     return "srwm_d64w2_kernel" if wl.B * wl.H > 2 * n_sm else "srwm_d64_kernel"
 
 

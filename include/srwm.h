@@ -74,13 +74,17 @@ int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, in
 /*
  * srwm_forward_balanced -- srwm_forward (same arguments, same results within
  * fp32 rounding) on a load-balanced schedule, for workloads with more
- * (sequence, head) streams than the GPU holds at once.  Every stream's T steps
- * are cut into segments (a multiple of 32 steps); a persistent cooperative
- * grid processes (stream, segment) items in segment-major order, handing each
- * stream's state from one segment to the next through W_final.  This replaces
- * a mostly empty last wave of whole streams by rounds of short segments.  The
- * recurrence itself is unchanged: the pages' Eqs. (1)-(5) are sequential in t
- * within a stream, and the segments of one stream run strictly in order.
+ * (sequence, head) streams than the GPU holds at once.  A persistent
+ * cooperative grid splits streams into segments and hands each stream's state
+ * from one segment to the next through W_final, replacing a mostly empty last
+ * wave of whole streams.  The d = 32 kernel takes a wrap-around schedule: all
+ * streams' steps are laid end to end and every warp slot takes an equal range
+ * of them, so a stream is split at most once, its first part running at the
+ * start of one slot and its last part at the end of the next.  The other
+ * kernels cut every stream into segments of a multiple of 32 steps and
+ * process (stream, segment) items in segment-major order.  The recurrence
+ * itself is unchanged: the pages' Eqs. (1)-(5) are sequential in t within a
+ * stream, and the segments of one stream run strictly in order.
  *
  *   workspace        device memory the call uses for per-stream progress
  *                    counters (zeroed by the call on `stream`); at least
@@ -301,9 +305,27 @@ int srwm_set_wait_limit_ns(long long limit_ns);
 int srwm_debug_skip_x_chunk(int chunk);
 
 /*
+ * srwm_debug_wrap_len, srwm_debug_wrap_pieces -- tests only: the wrap-around
+ * schedule of srwm_forward_balanced (d = 32) without a GPU.
+ * srwm_debug_wrap_len returns the steps per warp slot the library chooses for
+ * n_streams streams of T steps on `slots` slots with TMA chunks of tau steps
+ * (0 when the schedule does not apply: n_streams <= slots, or a size <= 0).
+ * srwm_debug_wrap_pieces lists, in the order the slot runs them, the pieces
+ * of slot `slot` under range length wrap_len: four ints per piece (stream,
+ * segment number 0 or 1, first step, number of steps) into out (room for
+ * max_pieces pieces, caller-owned).  It returns the number of pieces (which
+ * may exceed max_pieces; only the first max_pieces are written), or -1 for
+ * invalid arguments (n_streams or T <= 0, wrap_len < T, slot < 0).
+ */
+long long srwm_debug_wrap_len(long long n_streams, int T, long long slots, int tau);
+int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long long slot, int* out,
+                           int max_pieces);
+
+/*
  * srwm_debug_set_segment_len -- tests only: force the segment length (a
- * positive multiple of 32 steps) that srwm_forward_balanced uses; 0 restores
- * the automatic choice.  Returns SRWM_ERR_SHAPE for other values.
+ * positive multiple of 32 steps) that srwm_forward_balanced uses, on the
+ * segment schedule for every kernel; 0 restores the automatic choice.
+ * Returns SRWM_ERR_SHAPE for other values.
  */
 int srwm_debug_set_segment_len(int steps);
 

@@ -16,6 +16,7 @@ _LIB = None
 
 # Status codes of include/srwm.h
 SRWM_OK = 0
+SRWM_ERR_SHAPE = 2
 SRWM_ERR_TIMEOUT = 7
 
 EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noalloc",
@@ -23,7 +24,8 @@ EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noall
            "srwm_forward_host_workspace_bytes",
            "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes",
            "srwm_layer_forward", "srwm_layer_workspace_bytes", "srwm_debug_set_layer_gemm", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
-           "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_probe_fma")
+           "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_debug_wrap_len",
+           "srwm_debug_wrap_pieces", "srwm_probe_fma")
 
 
 class SrwmError(RuntimeError):
@@ -58,6 +60,10 @@ def _lib():
         lib.srwm_forward_balanced_noalloc.restype = I
         lib.srwm_debug_set_segment_len.argtypes = [I]
         lib.srwm_debug_set_segment_len.restype = I
+        lib.srwm_debug_wrap_len.argtypes = [LL, I, LL, I]
+        lib.srwm_debug_wrap_len.restype = LL
+        lib.srwm_debug_wrap_pieces.argtypes = [LL, I, LL, LL, P, I]
+        lib.srwm_debug_wrap_pieces.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward_from.restype = I
         lib.srwm_forward_host.argtypes = [P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]
@@ -181,6 +187,23 @@ def srwm_forward_balanced_noalloc(x, W0, n_lr, softmax_input, y_out, W_final, st
                                               _dev(W_final, "W_final", (B, H, m, d)), _stream_handle(stream))
     _check(rc, "srwm_forward_balanced_noalloc")
     return y_out, W_final
+
+
+def srwm_debug_wrap_len(n_streams: int, T: int, slots: int, tau: int) -> int:
+    """Steps per warp slot of the wrap-around schedule (0: not used)."""
+    return int(_lib().srwm_debug_wrap_len(int(n_streams), int(T), int(slots), int(tau)))
+
+
+def srwm_debug_wrap_pieces(n_streams: int, T: int, wrap_len: int, slot: int):
+    """The pieces of one slot under the wrap-around schedule, in run order:
+    a list of (stream, segment, first step, steps)."""
+    lib = _lib()
+    n = lib.srwm_debug_wrap_pieces(int(n_streams), int(T), int(wrap_len), int(slot), None, 0)
+    if n < 0:
+        raise SrwmError(SRWM_ERR_SHAPE, "srwm_debug_wrap_pieces")
+    buf = (ctypes.c_int * (4 * max(n, 1)))()
+    lib.srwm_debug_wrap_pieces(int(n_streams), int(T), int(wrap_len), int(slot), buf, n)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
 
 def srwm_debug_set_segment_len(steps: int) -> None:

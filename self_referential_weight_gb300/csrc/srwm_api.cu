@@ -216,6 +216,15 @@ int choose_seg_len(long long n_streams, int T, long long slots)
     return best_len;
 }
 
+// Range length of the wrap-around schedule: ceil(total / slots) steps rounded
+// up to whole TMA chunks.  With more streams than slots it is at least T.
+long long wrap_len_for(long long n_streams, int T, long long slots, int tau)
+{
+    const long long total = n_streams * T;
+    const long long per = (total + slots - 1) / slots;
+    return (per + tau - 1) / tau * tau;
+}
+
 // Shared body of srwm_forward (per_seq = 0) and srwm_step (per_seq = 1, T = 1).
 int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, int d, int n_lr,
         int smx, float* y, float* W_out, cudaStream_t stream, int* seg_done = nullptr,
@@ -267,6 +276,7 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
     kp.seg_len = T > 0 ? T : 1;
     kp.n_items = kp.n_streams;
     kp.seg_done = nullptr;
+    kp.wrap_len = 0;
     kp.emit = emit;
     kp.emit_stride = emit_stride;
     if (!seg_done) return launch(li, tx, ty, kp, pairs, 0, stream);
@@ -281,6 +291,21 @@ int run(const float* x, const float* W_init, int per_seq, int B, int T, int H, i
         // Nothing to balance when every stream has a slot of its own: the plain
         // launch (one stream per slot, spread over the SMs) is the fast one.
         if (pairs <= slots) return launch(li, tx, ty, kp, pairs, 0, stream);
+        if (li.wraps && T > 0) {
+            // wrap-around: every slot gets ceil(total / slots) steps, rounded up
+            // to whole TMA chunks (>= T, as there are more streams than slots)
+            const long long wrap = wrap_len_for(pairs, T, slots, li.tau);
+            const long long used = (pairs * T + wrap - 1) / wrap;
+            if (cudaMemsetAsync(seg_done, 0, seg_done_bytes, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return SRWM_ERR_CUDA;
+            }
+            kp.seg_done = seg_done;
+            kp.wrap_len = wrap;
+            kp.n_items = 0;
+            const long long need = (used + li.streams_per_cta - 1) / li.streams_per_cta;
+            return launch(li, tx, ty, kp, pairs, static_cast<int>(need < ctas ? need : ctas), stream);
+        }
         len = choose_seg_len(pairs, T, slots);
     }
     if (T <= 0 || len >= T) len = T > 0 ? T : 1;
@@ -424,6 +449,32 @@ int srwm_forward_balanced(const float* x, const float* W0, int B, int T, int H, 
     if (prc != SRWM_OK) return prc;
     return run(x, W0, 0, B, T, H, d, n_lr, softmax_input, y_out, W_final,
                static_cast<cudaStream_t>(stream), static_cast<int*>(workspace), need);
+}
+
+long long srwm_debug_wrap_len(long long n_streams, int T, long long slots, int tau)
+{
+    if (n_streams <= slots || T <= 0 || slots <= 0 || tau <= 0) return 0;
+    return wrap_len_for(n_streams, T, slots, tau);
+}
+
+int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long long slot, int* out, int max_pieces)
+{
+    if (n_streams <= 0 || T <= 0 || wrap_len < T || slot < 0 || max_pieces < 0 || (max_pieces > 0 && !out))
+        return -1;
+    const long long lo = slot * wrap_len;
+    long long hi = lo + wrap_len < n_streams * T ? lo + wrap_len : n_streams * T;
+    srwm::Piece pc;
+    int n = 0;
+    while (srwm::wrap_next(lo, hi, T, pc)) {
+        if (n < max_pieces) {
+            out[4 * n + 0] = pc.p;
+            out[4 * n + 1] = pc.seg;
+            out[4 * n + 2] = pc.t0;
+            out[4 * n + 3] = pc.len;
+        }
+        ++n;
+    }
+    return n;
 }
 
 int srwm_debug_set_segment_len(int steps)

@@ -31,6 +31,11 @@ struct KParams {
     int n_streams;                     // B * H
     int seg_len;                       // steps per item
     int n_items;                       // n_streams * segments
+    // > 0: the wrap-around schedule instead of segments (kernels whose
+    // LaunchInfo::wraps is set): slot k takes the positions
+    // [k * wrap_len, (k + 1) * wrap_len) of all streams' steps laid end to end
+    // (see wrap_next).
+    long long wrap_len;
     // Per-stream count of finished segments (only when streams span several
     // segments; NULL otherwise).  Segment s of a stream waits until its count
     // reaches s; its state comes from W_out, where segment s - 1 left it.
@@ -42,6 +47,33 @@ struct KParams {
     int emit_stride;   // floats per record, a multiple of 4
 };
 
+// One piece of a slot's work: steps t0 .. t0 + len - 1 of stream p, the
+// stream's segment number seg (its state comes from segment seg - 1).
+struct Piece {
+    int p, seg, t0, len;
+};
+
+// Wrap-around schedule.  Stream p's steps are the positions p*T .. p*T + T - 1
+// of one line; a slot owns the range [lo, hi) of that line and takes it in
+// pieces, last piece first: each call returns the piece that ends at hi and
+// moves hi to its start.  With ranges of at least T positions a stream falls
+// into at most two ranges.  Its first steps end one range and so run first on
+// that slot; its last steps begin the next range and so run last on the next
+// slot, and as the two parts add up to T <= range length, the second never
+// has to wait long for the first (segment 1 waits on segment 0's counter).
+SRWM_HD inline bool wrap_next(long long lo, long long& hi, int T, Piece& pc)
+{
+    if (hi <= lo || T <= 0) return false;
+    const long long p = (hi - 1) / T;
+    const long long start = lo > p * T ? lo : p * T;
+    pc.p = static_cast<int>(p);
+    pc.t0 = static_cast<int>(start - p * T);
+    pc.len = static_cast<int>(hi - start);
+    pc.seg = pc.t0 > 0 ? 1 : 0;
+    hi = start;
+    return true;
+}
+
 // Floats per backward record (see KParams::emit), rounded up to 16 bytes.
 SRWM_HD constexpr int emit_record_floats(int d, int n_lr) { return (2 * d + 4 + 3 * d + n_lr + 3) / 4 * 4; }
 
@@ -52,6 +84,7 @@ struct LaunchInfo {
     int streams_per_cta;  // (sequence, head) streams per CTA
     int smem_bytes;       // dynamic shared memory
     int tau;              // steps per TMA chunk (box height of the x / y tensor maps)
+    bool wraps;           // takes the wrap-around schedule (KParams::wrap_len)
 };
 
 // emit: the instantiation that also writes the backward records (KParams::emit).

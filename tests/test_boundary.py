@@ -26,7 +26,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(srwm_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|long long|const char\*)\s+(srwm_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():

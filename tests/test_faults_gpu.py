@@ -46,3 +46,31 @@ def test_missing_chunk_times_out_then_recovers(short_waits, d, B, smx):
     yo, Wo = oracle.forward(x, W0, 4, smx)
     assert np.abs(y.cpu().numpy() - yo).max() / np.abs(yo).max() <= 1e-4
     assert np.abs(Wf.cpu().numpy() - Wo).max() / np.abs(Wo).max() <= 1e-4
+
+
+def test_missing_chunk_wrap_schedule(short_waits):
+    """The d = 32 kernel on the wrap-around schedule (more streams than warp
+    slots): a missing chunk ends every slot with the timeout status, also the
+    slots whose next piece's chunks were already issued, and the next call
+    is correct."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    B = (12 * n_sm) // H + 7
+    wl = inputs.Workload("t", B, 100, H, 32, 1, True, 77, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
+    assert binding.srwm_last_device_status() == 0
+
+    binding.srwm_debug_skip_x_chunk(1)
+    binding.srwm_forward_balanced(xd, W0d, 1, True)
+    assert binding.srwm_last_device_status() == binding.SRWM_ERR_TIMEOUT
+    assert binding.srwm_last_device_status() == 0
+
+    binding.srwm_debug_skip_x_chunk(-1)
+    y, Wf = binding.srwm_forward_balanced(xd, W0d, 1, True)
+    assert binding.srwm_last_device_status() == 0
+    rng = np.random.default_rng(3)
+    for b in sorted(set(int(v) for v in rng.integers(0, B, 6)) | {0, B - 1}):
+        yo, Wo = oracle.forward(x[b:b + 1], W0, 1, True)
+        assert np.abs(y[b].cpu().numpy() - yo[0]).max() / np.abs(yo).max() <= 1e-4
+        assert np.abs(Wf[b].cpu().numpy() - Wo[0]).max() / np.abs(Wo).max() <= 1e-4

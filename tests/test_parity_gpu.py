@@ -362,6 +362,33 @@ def test_balanced_forced_segments_many_streams(n_lr, smx):
     assert rel(yb, yo) <= 1e-4 and rel(Wb, Wo) <= 1e-4
 
 
+@pytest.mark.parametrize("T", [70, 64, 1])
+@pytest.mark.parametrize("n_lr,smx", [(1, True), (4, False)])
+def test_balanced_wrap_schedule_d32(T, n_lr, smx):
+    """The d = 32 kernel's wrap-around schedule: more streams than warp slots,
+    each slot an equal range of all streams' steps.  T = 70 puts the split
+    points inside TMA chunks; T = 1 never splits.  Every stream is checked
+    against the plain launch and the oracle; results are deterministic."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    B = (12 * n_sm) // H + 7   # 12 warp slots per SM
+    wl = inputs.Workload("t", B, T, H, 32, n_lr, smx, 300 + T + n_lr, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = run_gpu(x, W0, n_lr, smx)
+    xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
+    yb, Wb = binding.srwm_forward_balanced(xd, W0d, n_lr, smx)
+    yb2, Wb2 = binding.srwm_forward_balanced(xd, W0d, n_lr, smx)
+    torch.cuda.synchronize()
+    assert binding.srwm_last_device_status() == 0
+    yb, Wb = yb.cpu().numpy(), Wb.cpu().numpy()
+    assert rel(yb, y) <= 1e-5 and rel(Wb, Wf) <= 1e-5
+    np.testing.assert_array_equal(yb, yb2.cpu().numpy())
+    np.testing.assert_array_equal(Wb, Wb2.cpu().numpy())
+    yo, Wo = oracle.forward(x, W0, n_lr, smx)
+    for b in range(B):
+        assert rel(yb[b], yo[b]) <= 1e-4 and rel(Wb[b], Wo[b]) <= 1e-4
+
+
 @pytest.mark.parametrize("name", ["mid", "rl", "fewshot"])
 def test_balanced_full_size_sampled(name):
     """The balanced schedule at full size with its automatic segment length;

@@ -1,0 +1,90 @@
+"""The wrap-around schedule of srwm_forward_balanced (d = 32), checked on the
+host through the library's own schedule functions (no GPU needed).
+
+The schedule lays every stream's T steps end to end and gives each warp slot
+an equal range of them, taken last piece first.  These tests check what makes
+it correct and fast: every (stream, step) is covered exactly once, a stream
+is split at most once, its first part is the first piece of one slot and its
+last part the last piece of the next slot, so the second part normally starts
+after the first has finished.
+"""
+import pytest
+
+from self_referential_weight_gb300 import binding
+
+CASES = [
+    (2048, 512, 1824, 16),   # rl on a 152-SM GB300: 512 x 4 streams, 12 warp slots per SM
+    (1852, 70, 1824, 16),    # ragged T: splits fall inside TMA chunks
+    (2049, 33, 2048, 16),
+    (5, 1000, 3, 16),
+    (100, 7, 30, 16),
+    (97, 1, 13, 16),         # one-step streams: never split
+    (64, 48, 63, 16),
+]
+
+
+def pieces_of(n, T, C, slots):
+    return [binding.srwm_debug_wrap_pieces(n, T, C, k) for k in range(slots)]
+
+
+@pytest.mark.parametrize("n,T,slots,tau", CASES)
+def test_wrap_len(n, T, slots, tau):
+    C = binding.srwm_debug_wrap_len(n, T, slots, tau)
+    assert C % tau == 0 and C >= T
+    assert C * slots >= n * T
+    assert (C - tau) * slots < n * T   # no whole chunk more than needed
+
+
+def test_wrap_len_not_used():
+    assert binding.srwm_debug_wrap_len(1824, 512, 1824, 16) == 0   # every stream has a slot
+    assert binding.srwm_debug_wrap_len(10, 0, 3, 16) == 0
+    assert binding.srwm_debug_wrap_len(10, 5, 0, 16) == 0
+
+
+@pytest.mark.parametrize("n,T,slots,tau", CASES)
+def test_wrap_pieces_cover_every_step_once(n, T, slots, tau):
+    C = binding.srwm_debug_wrap_len(n, T, slots, tau)
+    seen = [[] for _ in range(n)]
+    for k, pcs in enumerate(pieces_of(n, T, C, slots)):
+        assert sum(p[3] for p in pcs) <= C
+        for (p, seg, t0, ln) in pcs:
+            assert 0 <= p < n and ln > 0 and 0 <= t0 and t0 + ln <= T
+            seen[p].append((t0, ln, seg, k))
+    for p in range(n):
+        parts = sorted(seen[p])
+        assert parts[0][0] == 0 and len(parts) <= 2
+        assert sum(ln for (_, ln, _, _) in parts) == T
+        for i, (t0, ln, seg, _) in enumerate(parts):
+            assert seg == i
+            if i:
+                assert t0 == parts[i - 1][0] + parts[i - 1][1]
+
+
+@pytest.mark.parametrize("n,T,slots,tau", CASES)
+def test_wrap_split_streams_run_in_order(n, T, slots, tau):
+    """A split stream's first part opens its slot's run order and its last
+    part closes the next slot's, so with equal speed per step the last part
+    starts no earlier than the first ends (slots with at least T steps)."""
+    C = binding.srwm_debug_wrap_len(n, T, slots, tau)
+    all_pcs = pieces_of(n, T, C, slots)
+    where = {}
+    for k, pcs in enumerate(all_pcs):
+        start = 0
+        for i, (p, seg, t0, ln) in enumerate(pcs):
+            where[(p, seg)] = (k, i, start, ln, len(pcs), sum(q[3] for q in pcs))
+            start += ln
+    for (p, seg), (k, i, start, ln, npc, total) in where.items():
+        if seg == 1:
+            k0, i0, start0, ln0, _, _ = where[(p, 0)]
+            assert k == k0 + 1
+            assert i0 == 0 and i == npc - 1
+            if total >= T:
+                assert start >= start0 + ln0
+
+
+def test_wrap_pieces_invalid_arguments():
+    with pytest.raises(binding.SrwmError):
+        binding.srwm_debug_wrap_pieces(10, 5, 4, 0)   # range shorter than a stream
+    with pytest.raises(binding.SrwmError):
+        binding.srwm_debug_wrap_pieces(0, 5, 8, 0)
+    assert binding.srwm_debug_wrap_pieces(10, 5, 8, 7) == []   # past the last position
