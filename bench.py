@@ -40,7 +40,7 @@ L2_FLUSH_BYTES = 256 << 20        # > 129 MB L2
 # their hash matches the one recorded in it.
 KERNEL_SOURCES = {
     "srwm_d64_kernel": ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
-    "srwm_d64w2_kernel": ["srwm_d64w2.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
+    "srwm_d64r_kernel": ["srwm_d64r.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
     "srwm_d32_kernel": ["srwm_d32.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d32.cu"],
     "srwm_warp_kernel": ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h"],
 }
@@ -100,7 +100,7 @@ def kernel_name(wl, n_sm):
         return "srwm_warp_kernel"
     if wl.d == 32:
         return "srwm_d32_kernel"
-    return "srwm_d64w2_kernel" if wl.B * wl.H > 2 * n_sm else "srwm_d64_kernel"
+    return "srwm_d64r_kernel" if wl.B * wl.H > 2 * n_sm else "srwm_d64_kernel"
 
 
 def profile_summary_path(kernel, workload):

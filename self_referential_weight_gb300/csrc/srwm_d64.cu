@@ -1,7 +1,7 @@
 // srwm_d64.cu -- instantiations of the d = 64 kernels (one translation unit
 // per width so the library builds in parallel).
 #include "srwm_d64.cuh"
-#include "srwm_d64w2.cuh"
+#include "srwm_d64r.cuh"
 
 namespace srwm {
 
@@ -13,8 +13,8 @@ LaunchInfo pick(int n_lr, int softmax_input, bool two_warps)
     if constexpr (!EMIT) {
         if (two_warps) {
             if (n_lr == 1)
-                return softmax_input ? launch_info_d64w2_impl<1, true>() : launch_info_d64w2_impl<1, false>();
-            return softmax_input ? launch_info_d64w2_impl<4, true>() : launch_info_d64w2_impl<4, false>();
+                return softmax_input ? launch_info_d64r_impl<1, true>() : launch_info_d64r_impl<1, false>();
+            return softmax_input ? launch_info_d64r_impl<4, true>() : launch_info_d64r_impl<4, false>();
         }
     }
     if (n_lr == 1)
@@ -30,8 +30,8 @@ LaunchInfo pick(int n_lr, int softmax_input, bool two_warps)
 //     (Eight warps per stream, one stream per SM, was measured slower on the
 //     long workload: each warp reloads the step's vectors from shared memory,
 //     and that traffic grows with the warp count.)
-//   * more: two warps per stream, four CTAs per SM, so twice as many streams
-//     advance at once.
+//   * more: two warps per stream with whole rows of W per thread, four CTAs
+//     per SM, so twice as many streams advance at once.
 // emit selects the instantiations that also write the backward records: the
 // four-warp kernel at any stream count (the two-warp kernel has no registers
 // to spare for the record stores).
