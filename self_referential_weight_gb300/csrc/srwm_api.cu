@@ -579,7 +579,7 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
     if ((rc = run(x, W0, 0, B, T, H, d, n_lr, softmax_input, reinterpret_cast<float*>(base + w.y), WT, st,
                   reinterpret_cast<int*>(base + w.cnt), static_cast<size_t>(B) * H * 4, rec, stride)) != SRWM_OK)
         return rc;
-    // 2. the steps backwards, one CTA per stream
+    // 2. the steps backwards, one CTA per stream or per wrap-around range
     const srwm::BwdLaunch li = srwm::bwd_info(d, n_lr);
     if (cudaFuncSetAttribute(li.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, li.smem_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -597,11 +597,42 @@ int srwm_backward(const float* x, const float* W0, int B, int T, int H, int d, i
     bp.B = B;
     bp.T = T;
     bp.H = H;
+    bp.wrap_len = 0;
+    bp.seg_done = nullptr;
+    if ((rc = status_ptr(&bp.status)) != SRWM_OK) return rc;
+    bp.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
     int smx = softmax_input;
     void* args[] = {&bp, &smx};
-    if (cudaLaunchKernel(li.kernel, dim3(static_cast<unsigned>(static_cast<long long>(B) * H)),
-                         dim3(static_cast<unsigned>(li.threads)), args, static_cast<size_t>(li.smem_bytes),
-                         st) != cudaSuccess) {
+    // More streams than co-resident CTAs: the wrap-around schedule, so that the
+    // last wave is not mostly empty (each stream is split at most once).
+    const long long pairs = static_cast<long long>(B) * H;
+    int dev = 0, n_sm = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, li.kernel, li.threads,
+                                                      static_cast<size_t>(li.smem_bytes)) != cudaSuccess ||
+        per_sm <= 0) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    const long long slots = static_cast<long long>(n_sm) * per_sm;
+    cudaError_t e;
+    if (T > 0 && pairs > slots) {
+        bp.wrap_len = wrap_len_for(pairs, T, slots, li.kseg);
+        bp.seg_done = reinterpret_cast<int*>(base + w.cnt);
+        if (cudaMemsetAsync(bp.seg_done, 0, static_cast<size_t>(pairs) * 4, st) != cudaSuccess) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        const long long grid = (pairs * T + bp.wrap_len - 1) / bp.wrap_len;
+        e = cudaLaunchCooperativeKernel(li.kernel, dim3(static_cast<unsigned>(grid)),
+                                        dim3(static_cast<unsigned>(li.threads)), args,
+                                        static_cast<size_t>(li.smem_bytes), st);
+    } else {
+        e = cudaLaunchKernel(li.kernel, dim3(static_cast<unsigned>(pairs)), dim3(static_cast<unsigned>(li.threads)),
+                             args, static_cast<size_t>(li.smem_bytes), st);
+    }
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return SRWM_ERR_CUDA;
     }

@@ -44,7 +44,8 @@ namespace srwm {
 
 struct BwdParams {
     const float* x;        // [B, T, H, D]
-    const float* WT;       // [B, H, M, D]: W_T of every stream, from the forward pass
+    float* WT;             // [B, H, M, D]: W_T of every stream, from the forward pass (and a
+                           // split stream's hand-off of W, see wrap_len)
     const float* rec;      // the forward's per-step records (KParams::emit layout)
     int rec_stride;        // floats per record
     const float* dy;       // [B, T, H, D]
@@ -52,6 +53,14 @@ struct BwdParams {
     float* dx;             // [B, T, H, D]
     float* dW_seq;         // [B, H, M, D]: dL/dW0 of every stream (summed over b later)
     int B, T, H;
+    // > 0: the wrap-around schedule over the streams' steps taken backwards
+    // (position r of stream p is step T - 1 - r; see wrap_next).  A stream
+    // split in two hands W (through WT) and dL/dW (through dW_seq) from its
+    // later part to its earlier part, which waits on the stream's counter.
+    long long wrap_len;
+    int* seg_done;                     // per-stream counters (wrap schedule only)
+    unsigned* status;                  // device status word
+    unsigned long long wait_limit_ns;  // bounded-wait limit
 };
 
 template <int D_, int NLR_>
@@ -151,10 +160,8 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 2, cg = tid & 3;
-    const int p = blockIdx.x;
-    const int b = p / bp.H, h = p - b * bp.H;
+    int p = blockIdx.x, b = 0, h = 0;   // the current piece's stream
     const int T = bp.T;
-    const int nseg = cdiv(T, KSEG);
     const size_t MD = static_cast<size_t>(M) * D;
     auto blk = [](int r) { return NLR == 1 ? 0 : (r < 3 * D ? r / D : 3); };
     auto gidx = [&](int r) { return blk(r); };
@@ -269,24 +276,61 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
         __syncthreads();
     };
 
-    // ---- W_T (from the forward pass) and dL/dW_T
+    // ---- this CTA's pieces: one whole stream (plain launch), or the
+    // wrap-around schedule's pieces taken backwards in time
+    long long lo = 0, hi = 0;
+    if (bp.wrap_len > 0) {
+        lo = static_cast<long long>(blockIdx.x) * bp.wrap_len;
+        hi = min(lo + bp.wrap_len, static_cast<long long>(bp.B) * bp.H * T);
+    }
+    bool first = true;
+    for (;;) {
+        int t_lo = 0, t_hi = T, seg = 0;   // steps t_lo .. t_hi - 1 of stream p
+        if (bp.wrap_len > 0) {
+            Piece pc;
+            if (!wrap_next(lo, hi, T, pc)) break;
+            p = pc.p;
+            t_hi = T - pc.t0;
+            t_lo = t_hi - pc.len;
+            seg = pc.seg;
+        } else if (!first) {
+            break;
+        }
+        first = false;
+        b = p / bp.H;
+        h = p - b * bp.H;
+        if (seg > 0) {
+            int fail = 0;
+            if (tid == 0) fail = !wait_counter_bounded(bp.seg_done + p, seg, bp.wait_limit_ns);
+            if (__syncthreads_or(fail)) {
+                if (tid == 0) atomicOr(bp.status, kStatusTimeout);
+                return;
+            }
+        }
+
+    // ---- W at step t_hi (W_T from the forward pass, or where the later part
+    // of the stream left it) and dL/dW there
     load_state(bp.WT + static_cast<size_t>(p) * MD);
+    {
+        const float* dsrc = seg > 0 ? bp.dW_seq + static_cast<size_t>(p) * MD
+                                    : (bp.dWf != nullptr ? bp.dWf + static_cast<size_t>(p) * MD : nullptr);
 #pragma unroll
-    for (int i = 0; i < S; ++i) {
-        const int r = rg + RG * i;
+        for (int i = 0; i < S; ++i) {
+            const int r = rg + RG * i;
 #pragma unroll
-        for (int j = 0; j < C::NCH; ++j) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (bp.dWf != nullptr && r < M)
-                v = *reinterpret_cast<const float4*>(bp.dWf + static_cast<size_t>(p) * MD + static_cast<size_t>(r) * D + 4 * (cg + 4 * j));
-            dw[i][2 * j] = make_float2(v.x, v.y);
-            dw[i][2 * j + 1] = make_float2(v.z, v.w);
+            for (int j = 0; j < C::NCH; ++j) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (dsrc != nullptr && r < M)
+                    v = __ldcg(reinterpret_cast<const float4*>(dsrc + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)));
+                dw[i][2 * j] = make_float2(v.x, v.y);
+                dw[i][2 * j + 1] = make_float2(v.z, v.w);
+            }
         }
     }
     // ---- segments backwards; each step subtracts its recorded update from W
-    for (int j = nseg - 1; j >= 0; --j) {
-        const int t0 = j * KSEG;
-        const int len = min(KSEG, T - t0);
+    for (int top = t_hi; top > t_lo; top -= KSEG) {
+        const int t0 = max(t_lo, top - KSEG);
+        const int len = top - t0;
         stage(t0, len, true);
         // the forward's records of the segment: phi(k), u, gates, a.  float4
         // pieces (every field starts at a multiple of 4 floats), four loads in
@@ -458,6 +502,16 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
         __syncthreads();   // the segment's staged vectors are read before the next segment's staging
     }
     store_tile(dw, bp.dW_seq + static_cast<size_t>(p) * MD);
+    if (t_lo > 0) {
+        // the earlier part of the stream continues from here
+        store_tile(w, bp.WT + static_cast<size_t>(p) * MD);
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            st_release_gpu(bp.seg_done + p, seg + 1);
+        }
+    }
+    }
 }
 
 struct BwdLaunch {

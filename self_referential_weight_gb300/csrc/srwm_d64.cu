@@ -10,12 +10,10 @@ namespace {
 template <bool EMIT>
 LaunchInfo pick(int n_lr, int softmax_input, bool two_warps)
 {
-    if constexpr (!EMIT) {
-        if (two_warps) {
-            if (n_lr == 1)
-                return softmax_input ? launch_info_d64r_impl<1, true>() : launch_info_d64r_impl<1, false>();
-            return softmax_input ? launch_info_d64r_impl<4, true>() : launch_info_d64r_impl<4, false>();
-        }
+    if (two_warps) {
+        if (n_lr == 1)
+            return softmax_input ? launch_info_d64r_impl<1, true, EMIT>() : launch_info_d64r_impl<1, false, EMIT>();
+        return softmax_input ? launch_info_d64r_impl<4, true, EMIT>() : launch_info_d64r_impl<4, false, EMIT>();
     }
     if (n_lr == 1)
         return softmax_input ? launch_info_d64_impl<4, 1, true, EMIT>() : launch_info_d64_impl<4, 1, false, EMIT>();
@@ -32,9 +30,7 @@ LaunchInfo pick(int n_lr, int softmax_input, bool two_warps)
 //     and that traffic grows with the warp count.)
 //   * more: two warps per stream with whole rows of W per thread, four CTAs
 //     per SM, so twice as many streams advance at once.
-// emit selects the instantiations that also write the backward records: the
-// four-warp kernel at any stream count (the two-warp kernel has no registers
-// to spare for the record stores).
+// emit selects the instantiations that also write the backward records.
 LaunchInfo launch_info_d64(int n_lr, int softmax_input, long long n_streams, int n_sm, bool emit)
 {
     const bool two_warps = n_streams > 2LL * n_sm;

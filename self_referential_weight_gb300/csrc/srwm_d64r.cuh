@@ -34,7 +34,8 @@
 // Steps run chunk by chunk: waits, TMA loads and stores sit at chunk
 // boundaries, and with the input softmax the two warps replace a landed
 // chunk's rows by x~ in place there, so a step reads x~ straight from the
-// three-chunk x ring.
+// three-chunk x ring.  With records on (the forward of the
+// backward pass), step t also writes phi_k, u, the gates and the rows' a.
 #pragma once
 
 #include <cuda.h>
@@ -85,9 +86,10 @@ __device__ __forceinline__ float warp_allsum(float v)
 
 // One step (see the file comment).  coef/coefb and the phi_k buffer of the
 // previous step hold the pending update; on return they hold this step's.
-template <int NLR>
-__device__ __forceinline__ void d64r_step(d64r::Smem& sm, int t, int T, int tid, int lane, int warp,
-                                          float2 (&w)[3][d64r::NP], float4& wb, float (&coef)[3], float& coefb)
+template <int NLR, bool EMIT>
+__device__ __forceinline__ void d64r_step(d64r::Smem& sm, const KParams& kp, int p, int t, int T, int tid, int lane,
+                                          int warp, float2 (&w)[3][d64r::NP], float4& wb, float (&coef)[3],
+                                          float& coefb)
 {
     using namespace d64r;
     const float* zt = sm.z[t & 1];
@@ -109,6 +111,17 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, int t, int T, int tid,
     // q rows would no longer give u = 0 exactly
     u_cur[lane] = __fsub_rn(pq0, pk0);
     u_cur[lane + 32] = __fsub_rn(pq1, pk1);
+    // backward record of step t: phi(k), u, gates, a (the rows' a follow below)
+    float* em = nullptr;
+    if constexpr (EMIT) {
+        em = kp.emit + (static_cast<size_t>(p) * kp.T + sm.t0 + t) * kp.emit_stride;
+        if (warp == 0) {
+            em[lane] = pk0;
+            em[lane + 32] = pk1;
+            em[D + lane] = __fsub_rn(pq0, pk0);
+            em[D + lane + 32] = __fsub_rn(pq1, pk1);
+        }
+    }
     const float sp = fmaf(pk0, xn[lane], pk1 * xn[lane + 32]);
     const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
     __syncwarp();
@@ -173,6 +186,13 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, int t, int T, int tid,
         coef[i] = g[NLR == 1 ? 0 : i] * (aa[i].x + aa[i].y);
         zr[i] = fmaf(coef[i], s, bb[i].x + bb[i].y);
     }
+    if constexpr (EMIT) {
+        float* ea = em + 2 * D + 4;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) ea[D * i + tid] = aa[i].x + aa[i].y;
+        if ((tid & 15) == 0 && (tid >> 4) < NLR) ea[3 * D + (tid >> 4)] = abb;
+        if (tid < 4) em[2 * D + tid] = tid == 0 ? g[0] : tid == 1 ? g[1] : tid == 2 ? g[2] : g[3];
+    }
     if (t + 1 < T) sm.yring[(t + 1) % (3 * TAU)][tid] = zr[0];
     zn[D + tid] = zr[1];
     zn[2 * D + tid] = zr[2];
@@ -180,7 +200,7 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, int t, int T, int tid,
     if ((tid & 15) == 0 && (tid >> 4) < NLR) zn[3 * D + (tid >> 4)] = fmaf(coefb, s, bbb);
 }
 
-template <int NLR, bool SMX>
+template <int NLR, bool SMX, bool EMIT>
 __global__ void __launch_bounds__(d64r::NT, 4)
     srwm_d64r_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const KParams kp)
@@ -347,7 +367,7 @@ __global__ void __launch_bounds__(d64r::NT, 4)
             }
             const int t_end = min(T, (c + 1) * TAU);
             for (int t = c * TAU; t < t_end; ++t) {
-                d64r_step<NLR>(sm, t, T, tid, lane, warp, w, wb, coef, coefb);
+                d64r_step<NLR, EMIT>(sm, kp, p, t, T, tid, lane, warp, w, wb, coef, coefb);
                 __syncthreads();
             }
         }
@@ -407,10 +427,10 @@ __global__ void __launch_bounds__(d64r::NT, 4)
     }
 }
 
-template <int NLR, bool SMX>
+template <int NLR, bool SMX, bool EMIT = false>
 LaunchInfo launch_info_d64r_impl()
 {
-    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64r_kernel<NLR, SMX>), d64r::NT, 1,
+    return LaunchInfo{reinterpret_cast<const void*>(&srwm_d64r_kernel<NLR, SMX, EMIT>), d64r::NT, 1,
                       static_cast<int>(sizeof(d64r::Smem)) + 128, d64r::TAU};
 }
 

@@ -70,6 +70,31 @@ def test_backward_longer_sequence():
     check(inputs.Workload("g", 1, 400, 2, 64, 4, False, 600, "normal"))
 
 
+@pytest.mark.parametrize("T", [70, 33])
+def test_backward_wrap_schedule(T):
+    """More d = 64 streams than the backward kernel's co-resident CTAs (one per
+    SM) selects the wrap-around schedule: streams split in two hand W and
+    dL/dW from their later to their earlier part.  dL/dx equals, bit for bit,
+    two half-batch calls that each fit in one wave (W and dL/dW pass through
+    memory unchanged); dL/dW0 agrees within the rounding of the sum over b;
+    one head's gradients match the oracle."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    B = 2 * ((n_sm // H) // 2 + 4)   # > n_sm streams; each half <= n_sm
+    wl = inputs.Workload("g", B, T, H, 64, 4, False, 800 + T, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    dy, dWf = inputs.make_cotangents(wl, True)
+    dx, dW0 = run_bwd(x, W0, 4, False, dy, dWf)
+    hB = B // 2
+    dx1, dW01 = run_bwd(x[:hB], W0, 4, False, dy[:hB], dWf[:hB])
+    dx2, dW02 = run_bwd(x[hB:], W0, 4, False, dy[hB:], dWf[hB:])
+    np.testing.assert_array_equal(dx, np.concatenate([dx1, dx2]))
+    assert rel(dW0, dW01.astype(np.float64) + dW02) <= 1e-6
+    h = 1
+    ox, oW = srwm_grad.grads(x[:, :, h:h + 1], W0[h:h + 1], 4, False, dy[:, :, h:h + 1], dWf[:, h:h + 1])
+    assert rel(dx[:, :, h:h + 1], ox) <= TOL and rel(dW0[h:h + 1], oW) <= TOL
+
+
 @pytest.mark.parametrize("d", [16, 64])
 def test_backward_zero_steps(d):
     wl = inputs.Workload("g", 3, 0, 2, d, 4, False, 700, "normal")
