@@ -145,10 +145,12 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
 /*
  * srwm_forward_host -- srwm_forward with HOST buffers: x, W0 in host memory,
  * y and W_final written to host memory.  The copies overlap the recurrence:
- * the sequence is cut into chunks of chunk_steps steps (<= 0: 128).  The H2D
- * copy of chunk k+1 and the D2H copy of chunk k-1 run on the library's own copy
- * streams while chunk k runs on `stream`, the state passing between chunks as
- * in srwm_forward_from.  Results equal srwm_forward's within fp32 rounding (a
+ * the sequence is cut into chunks of chunk_steps steps, or, for chunk_steps
+ * <= 0, into chunks that double from 32 steps up to 256 and halve again at the
+ * end (the middle split evenly), so that the first H2D and the last D2H copy,
+ * which nothing overlaps, stay short.  The H2D copy of chunk k+1 and the D2H
+ * copy of chunk k-1 run on the library's own copy streams while chunk k runs
+ * on `stream`, the state passing between chunks as in srwm_forward_from.  Results equal srwm_forward's within fp32 rounding (a
  * chunk restarts its first read-out from the stored state).
  *
  *   x_host        [B, T, H, d]  host memory, page-locked (cudaHostAlloc /
@@ -157,7 +159,7 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
  *   W0_host       [H, m, d]     host memory
  *   y_host        [B, T, H, d]  host memory, written
  *   W_final_host  [B, H, m, d]  host memory, written
- *   chunk_steps   steps per chunk
+ *   chunk_steps   steps per chunk; <= 0: the doubling plan above
  *   workspace     DEVICE scratch of srwm_forward_host_workspace_bytes(...)
  *                 bytes, 16-byte aligned
  *
@@ -320,6 +322,15 @@ int srwm_debug_skip_x_chunk(int chunk);
 long long srwm_debug_wrap_len(long long n_streams, int T, long long slots, int tau);
 int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long long slot, int* out,
                            int max_pieces);
+
+/*
+ * srwm_debug_chunk_plan -- tests only: the chunk lengths srwm_forward_host
+ * uses for T steps and the given chunk_steps, in order, into out (room for
+ * max_chunks, caller-owned).  Returns the number of chunks (which may exceed
+ * max_chunks; only the first max_chunks are written), or -1 for T < 0,
+ * max_chunks < 0, or out NULL with max_chunks > 0.
+ */
+int srwm_debug_chunk_plan(int T, int chunk_steps, int* out, int max_chunks);
 
 /*
  * srwm_debug_set_segment_len -- tests only: force the segment length (a

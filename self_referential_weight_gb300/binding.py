@@ -25,7 +25,7 @@ EXPORTS = ("srwm_forward", "srwm_forward_balanced", "srwm_forward_balanced_noall
            "srwm_step", "srwm_backward", "srwm_backward_workspace_bytes",
            "srwm_layer_forward", "srwm_layer_workspace_bytes", "srwm_debug_set_layer_gemm", "srwm_status_string", "srwm_last_device_status", "srwm_set_wait_limit_ns",
            "srwm_debug_skip_x_chunk", "srwm_debug_set_segment_len", "srwm_debug_wrap_len",
-           "srwm_debug_wrap_pieces", "srwm_probe_fma")
+           "srwm_debug_wrap_pieces", "srwm_debug_chunk_plan", "srwm_probe_fma")
 
 
 class SrwmError(RuntimeError):
@@ -64,6 +64,8 @@ def _lib():
         lib.srwm_debug_wrap_len.restype = LL
         lib.srwm_debug_wrap_pieces.argtypes = [LL, I, LL, LL, P, I]
         lib.srwm_debug_wrap_pieces.restype = I
+        lib.srwm_debug_chunk_plan.argtypes = [I, I, P, I]
+        lib.srwm_debug_chunk_plan.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward_from.restype = I
         lib.srwm_forward_host.argtypes = [P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]
@@ -204,6 +206,17 @@ def srwm_debug_wrap_pieces(n_streams: int, T: int, wrap_len: int, slot: int):
     buf = (ctypes.c_int * (4 * max(n, 1)))()
     lib.srwm_debug_wrap_pieces(int(n_streams), int(T), int(wrap_len), int(slot), buf, n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def srwm_debug_chunk_plan(T: int, chunk_steps: int = 0):
+    """The chunk lengths srwm_forward_host uses for T steps."""
+    lib = _lib()
+    n = lib.srwm_debug_chunk_plan(int(T), int(chunk_steps), None, 0)
+    if n < 0:
+        raise SrwmError(SRWM_ERR_SHAPE, "srwm_debug_chunk_plan")
+    buf = (ctypes.c_int * max(n, 1))()
+    lib.srwm_debug_chunk_plan(int(T), int(chunk_steps), buf, n)
+    return list(buf[:n])
 
 
 def srwm_debug_set_segment_len(steps: int) -> None:

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "srwm.h"
 #include "srwm_common.h"
@@ -405,7 +406,41 @@ bool host_ws(long long B, long long T, long long H, long long d, long long n_lr,
     return true;
 }
 
-int effective_chunk(int T, int chunk_steps) { return chunk_steps > 0 ? (chunk_steps < T ? chunk_steps : (T > 0 ? T : 1)) : (T < 128 ? (T > 0 ? T : 1) : 128); }
+// Chunk plan of srwm_forward_host.  chunk_steps > 0: chunks of that many steps
+// (the last one ragged).  0: chunks that double from 32 steps up to 256 and
+// halve again at the end, the middle split evenly, so that the first input
+// copy and the last output copy (which nothing overlaps) stay short while
+// there are few launches.
+std::vector<int> chunk_plan(int T, int chunk_steps)
+{
+    std::vector<int> plan;
+    if (T <= 0) return plan;
+    if (chunk_steps > 0) {
+        for (int t = 0; t < T; t += chunk_steps) plan.push_back(T - t < chunk_steps ? T - t : chunk_steps);
+        return plan;
+    }
+    constexpr int kMin = 32, kMax = 256;
+    std::vector<int> tail;
+    int rem = T;
+    for (int c = kMin; c < kMax && rem >= 2 * c; c *= 2) {
+        plan.push_back(c);
+        tail.push_back(c);
+        rem -= 2 * c;
+    }
+    if (rem > 0) {
+        const int n = (rem + kMax - 1) / kMax;
+        for (int i = 0; i < n; ++i) plan.push_back(rem / n + (i < rem % n ? 1 : 0));
+    }
+    plan.insert(plan.end(), tail.rbegin(), tail.rend());
+    return plan;
+}
+
+int effective_chunk(int T, int chunk_steps)
+{
+    int c = 1;
+    for (int v : chunk_plan(T, chunk_steps)) c = v > c ? v : c;
+    return c;
+}
 
 }  // namespace
 
@@ -475,6 +510,14 @@ int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long 
         ++n;
     }
     return n;
+}
+
+int srwm_debug_chunk_plan(int T, int chunk_steps, int* out, int max_chunks)
+{
+    if (T < 0 || max_chunks < 0 || (max_chunks > 0 && !out)) return -1;
+    const std::vector<int> plan = chunk_plan(T, chunk_steps);
+    for (int i = 0; i < static_cast<int>(plan.size()) && i < max_chunks; ++i) out[i] = plan[i];
+    return static_cast<int>(plan.size());
 }
 
 int srwm_debug_set_segment_len(int steps)
@@ -694,9 +737,10 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
     if (T == 0) {
         if ((rc = run(nullptr, W0d, 0, B, 0, H, d, n_lr, softmax_input, nullptr, S, sc)) != SRWM_OK) return rc;
     }
-    const int K = T > 0 ? (T + C - 1) / C : 0;
-    for (int k = 0; k < K; ++k) {
-        const int slot = k % kPipeSlots, t0 = k * C, Ck = (T - t0 < C) ? T - t0 : C;
+    const std::vector<int> plan = chunk_plan(T, chunk_steps);
+    const int K = static_cast<int>(plan.size());
+    for (int k = 0, t0 = 0; k < K; t0 += plan[k], ++k) {
+        const int slot = k % kPipeSlots, Ck = plan[k];
         float* xb = reinterpret_cast<float*>(base + w.x[slot]);
         float* yb = reinterpret_cast<float*>(base + w.y[slot]);
         // x chunk k: host [B, T, H, d] rows t0 .. t0+Ck-1 -> contiguous [B, Ck, H, d]

@@ -85,3 +85,17 @@ def test_host_pipeline_rejects_device_memory():
     rc = lib.srwm_forward_host(xd.data_ptr(), torch.from_numpy(W0).data_ptr(), 2, 8, 2, 16, 4, 0, y.data_ptr(),
                                Wf.data_ptr(), 0, ws.data_ptr(), ws.numel(), None)
     assert rc == 3
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 200, 700])
+def test_host_pipeline_doubling_plan(T):
+    """The default chunk plan (doubling from 32 steps, halving at the end) over
+    several lengths equals srwm_forward within fp32 rounding."""
+    wl = inputs.Workload("t", 2, T, 2, 32, 1, True, 900 + T, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    y, Wf = host_forward(x, W0, 1, True, 0)
+    yd, Wd = binding.srwm_forward(torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV), 1, True)
+    torch.cuda.synchronize()
+    yd, Wd = yd.cpu().numpy(), Wd.cpu().numpy()
+    assert np.abs(y - yd).max() <= 1e-5 * np.abs(yd).max()
+    assert np.abs(Wf - Wd).max() <= 1e-5 * np.abs(Wd).max()

@@ -88,3 +88,32 @@ def test_wrap_pieces_invalid_arguments():
     with pytest.raises(binding.SrwmError):
         binding.srwm_debug_wrap_pieces(0, 5, 8, 0)
     assert binding.srwm_debug_wrap_pieces(10, 5, 8, 7) == []   # past the last position
+
+
+# ---------------------------------------------------------------- host pipeline chunk plan
+
+@pytest.mark.parametrize("T", [0, 1, 31, 63, 64, 65, 75, 200, 512, 1024, 1500, 8192])
+def test_chunk_plan_doubling(T):
+    """chunk_steps <= 0: chunks double from 32 steps up to at most 256 and halve
+    again at the end, the middle split evenly; they cover the T steps in
+    order.  Short first and last chunks keep the copies that nothing overlaps
+    short."""
+    plan = binding.srwm_debug_chunk_plan(T, 0)
+    assert sum(plan) == T and all(c > 0 for c in plan)
+    if T == 0:
+        assert plan == []
+        return
+    assert max(plan) <= 256
+    ramp = 0
+    while ramp < len(plan) // 2 and plan[ramp] == 32 << ramp and plan[-1 - ramp] == 32 << ramp:
+        ramp += 1
+    mid = plan[ramp:len(plan) - ramp]
+    assert not mid or max(mid) - min(mid) <= 1   # the middle split evenly
+    if T >= 64:
+        assert plan[0] == 32 and plan[-1] == 32
+
+
+@pytest.mark.parametrize("T,c", [(75, 32), (64, 64), (100, 1), (5, 128)])
+def test_chunk_plan_fixed(T, c):
+    plan = binding.srwm_debug_chunk_plan(T, c)
+    assert sum(plan) == T and all(v == c for v in plan[:-1]) and 0 < plan[-1] <= c
