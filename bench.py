@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
     "srwm_d64_kernel": ["srwm_d64.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
     "srwm_d64r_kernel": ["srwm_d64r.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d64.cu"],
     "srwm_d32_kernel": ["srwm_d32.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d32.cu"],
-    "srwm_warp_kernel": ["srwm_kernels.cuh", "srwm_ptx.cuh", "srwm_common.h"],
+    "srwm_d16_kernel": ["srwm_d16r.cuh", "srwm_ptx.cuh", "srwm_common.h", "srwm_d16.cu"],
 }
 
 
@@ -97,7 +97,7 @@ def kernel_name(wl, n_sm):
     """The kernel the library launches for this workload (see srwm_d32.cu and
     srwm_d64.cu)."""
     if wl.d == 16:
-        return "srwm_warp_kernel"
+        return "srwm_d16_kernel"
     if wl.d == 32:
         return "srwm_d32_kernel"
     return "srwm_d64r_kernel" if wl.B * wl.H > 2 * n_sm else "srwm_d64_kernel"
