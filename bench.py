@@ -366,10 +366,12 @@ def main():
            "h2d_bytes_per_step": x_h.numel() * 4 + W0_h.numel() * 4,
            "d2h_bytes_per_step": y_h.numel() * 4 + Wf_h.numel() * 4,
            "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "api": "srwm_forward_host (chunks doubling from 32 to at most 256 steps, halving at the end)"}
-    # the host results agree with the device path's (chunk restarts change fp32 rounding only)
+    # the host results agree with the device path's (chunk restarts change fp32
+    # rounding only), within the parity bar for this length
     y_dev = y.cpu()
-    if float((y_h - y_dev).abs().max()) > 1e-4 * float(y_dev.abs().max()):
-        raise RuntimeError("e2e host results differ from the device results")
+    e2e_dev = float((y_h - y_dev).abs().max()) / float(y_dev.abs().max())
+    if e2e_dev > (1e-4 if wl.T <= 1024 else 1e-3):
+        raise RuntimeError(f"e2e host results differ from the device results: {e2e_dev:.3g} relative")
 
     # ---------------- FMA probe (calibration of the FP32 roofline)
     props = torch.cuda.get_device_properties(dev)

@@ -48,15 +48,15 @@ def test_missing_chunk_times_out_then_recovers(short_waits, d, B, smx):
     assert np.abs(Wf.cpu().numpy() - Wo).max() / np.abs(Wo).max() <= 1e-4
 
 
-def test_missing_chunk_wrap_schedule(short_waits):
-    """The d = 32 kernel on the wrap-around schedule (more streams than warp
-    slots): a missing chunk ends every slot with the timeout status, also the
-    slots whose next piece's chunks were already issued, and the next call
-    is correct."""
+@pytest.mark.parametrize("d,H,slots_per_sm", [(32, 4, 12), (16, 16, 16)])
+def test_missing_chunk_wrap_schedule(short_waits, d, H, slots_per_sm):
+    """The d = 32 and d = 16 kernels on the wrap-around schedule (more streams
+    than warp slots): a missing chunk ends every slot with the timeout status,
+    also the slots whose next piece's chunks were already issued, and the next
+    call is correct."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    H = 4
-    B = (12 * n_sm) // H + 7
-    wl = inputs.Workload("t", B, 100, H, 32, 1, True, 77, "normal")
+    B = (slots_per_sm * n_sm) // H + 7
+    wl = inputs.Workload("t", B, 100, H, d, 1, True, 77 + d, "normal")
     x, W0 = inputs.make_inputs(wl)
     xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
     assert binding.srwm_last_device_status() == 0

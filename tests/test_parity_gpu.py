@@ -364,15 +364,16 @@ def test_balanced_forced_segments_many_streams(n_lr, smx):
 
 @pytest.mark.parametrize("T", [70, 64, 1])
 @pytest.mark.parametrize("n_lr,smx", [(1, True), (4, False)])
-def test_balanced_wrap_schedule_d32(T, n_lr, smx):
-    """The d = 32 kernel's wrap-around schedule: more streams than warp slots,
-    each slot an equal range of all streams' steps.  T = 70 puts the split
-    points inside TMA chunks; T = 1 never splits.  Every stream is checked
-    against the plain launch and the oracle; results are deterministic."""
+@pytest.mark.parametrize("d,H,slots_per_sm", [(32, 4, 12), (16, 16, 16)])
+def test_balanced_wrap_schedule(d, H, slots_per_sm, T, n_lr, smx):
+    """The d = 32 and d = 16 kernels' wrap-around schedule: more streams than
+    warp slots, each slot an equal range of all streams' steps.  T = 70 puts
+    the split points inside TMA chunks; T = 1 never splits.  Every stream is
+    checked against the plain launch and the oracle; results are
+    deterministic."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    H = 4
-    B = (12 * n_sm) // H + 7   # 12 warp slots per SM
-    wl = inputs.Workload("t", B, T, H, 32, n_lr, smx, 300 + T + n_lr, "normal")
+    B = (slots_per_sm * n_sm) // H + 7   # warp slots per SM: 12 (d = 32), 16 (d = 16)
+    wl = inputs.Workload("t", B, T, H, d, n_lr, smx, 300 + T + n_lr + d, "normal")
     x, W0 = inputs.make_inputs(wl)
     y, Wf = run_gpu(x, W0, n_lr, smx)
     xd, W0d = torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV)
