@@ -407,10 +407,10 @@ bool host_ws(long long B, long long T, long long H, long long d, long long n_lr,
 }
 
 // Chunk plan of srwm_forward_host.  chunk_steps > 0: chunks of that many steps
-// (the last one ragged).  0: chunks that double from 32 steps up to 256 and
-// halve again at the end, the middle split evenly, so that the first input
-// copy and the last output copy (which nothing overlaps) stay short while
-// there are few launches.
+// (the last one ragged).  0: chunks that double from 32 steps up to 256 (or
+// T / 8 for longer sequences) and halve again at the end, the middle split
+// evenly, so that the first input copy and the last output copy (which
+// nothing overlaps) stay short while there are few launches.
 std::vector<int> chunk_plan(int T, int chunk_steps)
 {
     std::vector<int> plan;
@@ -419,7 +419,8 @@ std::vector<int> chunk_plan(int T, int chunk_steps)
         for (int t = 0; t < T; t += chunk_steps) plan.push_back(T - t < chunk_steps ? T - t : chunk_steps);
         return plan;
     }
-    constexpr int kMin = 32, kMax = 256;
+    constexpr int kMin = 32;
+    const int kMax = T / 8 > 256 ? T / 8 : 256;
     std::vector<int> tail;
     int rem = T;
     for (int c = kMin; c < kMax && rem >= 2 * c; c *= 2) {

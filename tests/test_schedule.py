@@ -94,16 +94,16 @@ def test_wrap_pieces_invalid_arguments():
 
 @pytest.mark.parametrize("T", [0, 1, 31, 63, 64, 65, 75, 200, 512, 1024, 1500, 8192])
 def test_chunk_plan_doubling(T):
-    """chunk_steps <= 0: chunks double from 32 steps up to at most 256 and halve
-    again at the end, the middle split evenly; they cover the T steps in
-    order.  Short first and last chunks keep the copies that nothing overlaps
-    short."""
+    """chunk_steps <= 0: chunks double from 32 steps up to at most
+    max(256, T / 8) and halve again at the end, the middle split evenly; they
+    cover the T steps in order.  Short first and last chunks keep the copies
+    that nothing overlaps short."""
     plan = binding.srwm_debug_chunk_plan(T, 0)
     assert sum(plan) == T and all(c > 0 for c in plan)
     if T == 0:
         assert plan == []
         return
-    assert max(plan) <= 256
+    assert max(plan) <= max(256, T // 8)
     ramp = 0
     while ramp < len(plan) // 2 and plan[ramp] == 32 << ramp and plan[-1 - ramp] == 32 << ramp:
         ramp += 1
