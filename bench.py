@@ -94,8 +94,8 @@ def fmas_per_head_token(wl):
 
 
 def kernel_name(wl, n_sm):
-    """The kernel the library launches for this workload (see srwm_d32.cu and
-    srwm_d64.cu)."""
+    """The kernel the library launches for this workload (see srwm_d16.cu,
+    srwm_d32.cu and srwm_d64.cu)."""
     if wl.d == 16:
         return "srwm_d16_kernel"
     if wl.d == 32:
