@@ -149,8 +149,15 @@ __device__ __forceinline__ void warp_softmax_bwd(const float* s, const float* gi
     for (int c = lane; c < D; c += 32) out[c] = s[c] * (gin[c] - dot);
 }
 
+// Co-resident CTAs per SM the register budget is sized for: one at d = 64
+// (W and dL/dW fill the registers), three at d = 32 and eight at d = 16, which
+// fit without spills and hide more latency than the unconstrained allocation
+// (measured on rl: 4.28 -> 3.59 ms for the whole backward call).
+template <int D>
+constexpr int bwd_ctas_per_sm() { return D == 32 ? 3 : (D == 16 ? 8 : 1); }
+
 template <int D, int NLR>
-__global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, 1)
+__global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
     srwm_bwd_kernel(const BwdParams bp, int softmax_input)
 {
     using C = BwdCfg<D, NLR>;
