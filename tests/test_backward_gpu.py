@@ -71,17 +71,19 @@ def test_backward_longer_sequence():
 
 
 @pytest.mark.parametrize("T", [70, 33])
-def test_backward_wrap_schedule(T):
-    """More d = 64 streams than the backward kernel's co-resident CTAs (one per
-    SM) selects the wrap-around schedule: streams split in two hand W and
-    dL/dW from their later to their earlier part.  dL/dx equals, bit for bit,
-    two half-batch calls that each fit in one wave (W and dL/dW pass through
-    memory unchanged); dL/dW0 agrees within the rounding of the sum over b;
-    one head's gradients match the oracle."""
+@pytest.mark.parametrize("d,ctas_per_sm", [(64, 1), (32, 3), (16, 8)])
+def test_backward_wrap_schedule(d, ctas_per_sm, T):
+    """More streams than the backward kernel's co-resident CTAs (one, three or
+    eight per SM for d = 64, 32, 16) selects the wrap-around schedule: streams
+    split in two hand W and dL/dW from their later to their earlier part.
+    dL/dx equals, bit for bit, two half-batch calls that each fit in one wave
+    (W and dL/dW pass through memory unchanged); dL/dW0 agrees within the
+    rounding of the sum over b; one head's gradients match the oracle."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     H = 4
-    B = 2 * ((n_sm // H) // 2 + 4)   # > n_sm streams; each half <= n_sm
-    wl = inputs.Workload("g", B, T, H, 64, 4, False, 800 + T, "normal")
+    slots = ctas_per_sm * n_sm
+    B = 2 * ((slots // H) // 2 + 4)   # > slots streams; each half <= slots
+    wl = inputs.Workload("g", B, T, H, d, 4, False, 800 + T + d, "normal")
     x, W0 = inputs.make_inputs(wl)
     dy, dWf = inputs.make_cotangents(wl, True)
     dx, dW0 = run_bwd(x, W0, 4, False, dy, dWf)
