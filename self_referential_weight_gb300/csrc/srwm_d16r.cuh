@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(d16::Cfg<NLR, SMX>::NT, 2)
                 for (int r = 0; r < TAU / 2; ++r) v[r] = d16::softmax16(v[r]);
 #pragma unroll
                 for (int r = 0; r < TAU / 2; ++r) sm.xring[bi * TAU + 2 * r + (lane >> 4)][col] = v[r];
+                // the buffer is refilled by TMA later: order these writes first
+                fence_proxy_async_smem();
             }
             return true;
         };

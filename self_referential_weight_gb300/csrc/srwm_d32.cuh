@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(d32::Cfg<NLR, SMX>::NT, 2)
                 for (int r = 0; r < TAU; ++r) v[r] = d32::softmax32(v[r]);
 #pragma unroll
                 for (int r = 0; r < TAU; ++r) sm.xring[bi * TAU + r][lane] = v[r];
+                // the buffer is refilled by TMA later: order these writes first
+                fence_proxy_async_smem();
             }
             return true;
         };

@@ -252,6 +252,8 @@ __global__ void __launch_bounds__(d64r::NT, 4)
                 row[lane] = v0;
                 row[lane + 32] = v1;
             }
+            // the buffer is refilled by TMA later: order these writes first
+            fence_proxy_async_smem();
         }
         __syncthreads();
         if (tid == 0) {
