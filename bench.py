@@ -343,7 +343,7 @@ def main():
     W0_h = torch.from_numpy(W0_np).pin_memory()
     y_h = torch.empty(x_h.shape, dtype=torch.float32).pin_memory()
     Wf_h = torch.empty(tuple(Wf.shape), dtype=torch.float32).pin_memory()
-    chunk = 0   # the library's plan: chunks doubling from 32 steps up to 256, halving again at the end
+    chunk = 0   # the library's plan: chunks doubling from 32 steps, an even middle, halving again at the end
     host_ws = torch.empty(binding.srwm_forward_host_workspace_bytes(wl.B, wl.T, wl.H, wl.d, wl.n_lr, chunk),
                           dtype=torch.uint8, device=dev)
 
@@ -365,7 +365,7 @@ def main():
     e2e = {"value": world * ht_per_step * args.e2e_steps / t_e2e, "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * 4 + W0_h.numel() * 4,
            "d2h_bytes_per_step": y_h.numel() * 4 + Wf_h.numel() * 4,
-           "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "api": "srwm_forward_host (chunks doubling from 32 to at most 256 steps, halving at the end)"}
+           "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "api": "srwm_forward_host (chunks doubling from 32 steps, an even middle of at most max(256, T/8), halving at the end)"}
     # the host results agree with the device path's (chunk restarts change fp32
     # rounding only), within the parity bar for this length
     y_dev = y.cpu()

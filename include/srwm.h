@@ -146,9 +146,11 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
  * srwm_forward_host -- srwm_forward with HOST buffers: x, W0 in host memory,
  * y and W_final written to host memory.  The copies overlap the recurrence:
  * the sequence is cut into chunks of chunk_steps steps, or, for chunk_steps
- * <= 0, into chunks that double from 32 steps up to max(256, T / 8) and halve
- * again at the end (the middle split evenly), so that the first H2D and the
- * last D2H copy, which nothing overlaps, stay short.  The H2D copy of chunk k+1 and the D2H
+ * <= 0, into chunks that double from 32 steps and halve again at the end,
+ * with the middle split evenly into chunks of at most max(256, T / 8) steps
+ * (a ramp chunk is added on both ends while at least as many steps remain
+ * between them, up to half that size), so that the first H2D and the last D2H
+ * copy, which nothing overlaps, stay short.  T < 96 is a single chunk.  The H2D copy of chunk k+1 and the D2H
  * copy of chunk k-1 run on the library's own copy streams while chunk k runs
  * on `stream`, the state passing between chunks as in srwm_forward_from.  Results equal srwm_forward's within fp32 rounding (a
  * chunk restarts its first read-out from the stored state).

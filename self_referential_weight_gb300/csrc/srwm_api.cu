@@ -423,7 +423,11 @@ std::vector<int> chunk_plan(int T, int chunk_steps)
     const int kMax = T / 8 > 256 ? T / 8 : 256;
     std::vector<int> tail;
     int rem = T;
-    for (int c = kMin; c < kMax && rem >= 2 * c; c *= 2) {
+    // A ramp chunk goes on both ends while at least as much is left between
+    // them, and only up to half the largest chunk: the middle, split evenly into
+    // chunks of at most kMax, then never falls below the last ramp chunk, so the
+    // chunk sizes rise and then fall.
+    for (int c = kMin; 2 * c <= kMax && rem >= 3 * c; c *= 2) {
         plan.push_back(c);
         tail.push_back(c);
         rem -= 2 * c;

@@ -14,7 +14,8 @@
 // reach every lane as broadcast shared-memory reads, and k_t, q_t stay in the
 // registers of the lane that produced them until the next step's softmax.
 // Only the beta rows (one column per lane) and s = phi(k_t) . x~_{t+1} are
-// summed over the warp.
+// summed over the warp (with four beta rows, their eight sums by a
+// reduce-scatter butterfly).
 //
 // One step t, on W_{t-1} in registers:
 //   a_r       = W[r,:] . u_t                  (Eq. (2))
@@ -62,6 +63,33 @@ __device__ __forceinline__ void allsum(float (&v)[K])
 #pragma unroll
         for (int k = 0; k < K; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
     }
+}
+
+// Sums eight values over the 32 lanes by a reduce-scatter butterfly (each
+// level halves the values a lane carries), then broadcasts: value i ends fully
+// summed in lanes 4i..4i+3 and reaches every lane from lane 4i, so all lanes
+// get the same bits.  17 shuffles instead of 40.
+__device__ __forceinline__ void allsum8(float (&v)[8], int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w[4], x[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b4 ? v[j] : v[4 + j];
+        const float keep = b4 ? v[4 + j] : v[j];
+        w[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b3 ? w[j] : w[2 + j];
+        const float keep = b3 ? w[2 + j] : w[j];
+        x[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __shfl_sync(0xffffffffu, y, 4 * i);
 }
 
 template <int NLR_, bool SMX_>
@@ -311,7 +339,19 @@ __global__ void __launch_bounds__(d32::Cfg<NLR, SMX>::NT, 2)
                     red[1 + NLR + r] = wb[r] * xc;
                 }
                 __syncwarp();
-                d32::allsum(red);
+                if constexpr (NLR == 4) {
+                    float sv[1] = {red[0]};
+                    float bv[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) bv[r] = red[1 + r];
+                    d32::allsum(sv);
+                    d32::allsum8(bv, lane);
+                    red[0] = sv[0];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) red[1 + r] = bv[r];
+                } else {
+                    d32::allsum(red);
+                }
                 // one pass over W: the pending update of step t - 1 (Eq. (3)),
                 // then a = W u_t and b = W x~_{t+1} on the updated columns
                 const float* pkp = sm.pk[pp];

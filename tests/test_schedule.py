@@ -92,12 +92,12 @@ def test_wrap_pieces_invalid_arguments():
 
 # ---------------------------------------------------------------- host pipeline chunk plan
 
-@pytest.mark.parametrize("T", [0, 1, 31, 63, 64, 65, 75, 200, 512, 1024, 1500, 8192])
+@pytest.mark.parametrize("T", [0, 1, 31, 63, 64, 65, 75, 95, 96, 200, 512, 1024, 1500, 2056, 8192])
 def test_chunk_plan_doubling(T):
-    """chunk_steps <= 0: chunks double from 32 steps up to at most
-    max(256, T / 8) and halve again at the end, the middle split evenly; they
-    cover the T steps in order.  Short first and last chunks keep the copies
-    that nothing overlaps short."""
+    """chunk_steps <= 0: chunks double from 32 steps up to at most half of
+    max(256, T / 8) and halve again at the end, the middle split evenly into
+    chunks of at most max(256, T / 8); they cover the T steps in order.  Short
+    first and last chunks keep the copies that nothing overlaps short."""
     plan = binding.srwm_debug_chunk_plan(T, 0)
     assert sum(plan) == T and all(c > 0 for c in plan)
     if T == 0:
@@ -109,8 +109,22 @@ def test_chunk_plan_doubling(T):
         ramp += 1
     mid = plan[ramp:len(plan) - ramp]
     assert not mid or max(mid) - min(mid) <= 1   # the middle split evenly
-    if T >= 64:
+    if T >= 96:   # room for a 32-step chunk at both ends and as much between them
         assert plan[0] == 32 and plan[-1] == 32
+    else:
+        assert plan == [T]
+
+
+def test_chunk_plan_rises_then_falls():
+    """chunk_steps <= 0: over every length up to 4,096 steps (and some longer
+    ones) the chunks never shrink and then grow again, so a chunk whose copies
+    nothing overlaps is never in the middle of the call."""
+    for T in list(range(1, 4097)) + [6000, 8192, 10000, 65536]:
+        plan = binding.srwm_debug_chunk_plan(T, 0)
+        assert sum(plan) == T
+        top = plan.index(max(plan))
+        assert all(a <= b for a, b in zip(plan[:top], plan[1:top + 1])), (T, plan)
+        assert all(a >= b for a, b in zip(plan[top:], plan[top + 1:])), (T, plan)
 
 
 @pytest.mark.parametrize("T,c", [(75, 32), (64, 64), (100, 1), (5, 128)])
