@@ -148,9 +148,11 @@ int srwm_forward_from(const float* x, const float* W_init, int B, int T, int H, 
  * the sequence is cut into chunks of chunk_steps steps, or, for chunk_steps
  * <= 0, into chunks that double from 32 steps and halve again at the end,
  * with the middle split evenly into chunks of at most max(256, T / 8) steps
- * (a ramp chunk is added on both ends while at least as many steps remain
- * between them, up to half that size), so that the first H2D and the last D2H
- * copy, which nothing overlaps, stay short.  T < 96 is a single chunk.  The H2D copy of chunk k+1 and the D2H
+ * at d = 64 and 64 steps at d <= 32, where the copies rather than the
+ * recurrence set the pace (a ramp chunk is added on both ends while at least
+ * as many steps remain between them, up to half that size), so that the first
+ * H2D and the last D2H copy, which nothing overlaps, stay short.  T < 96 is a
+ * single chunk.  The H2D copy of chunk k+1 and the D2H
  * copy of chunk k-1 run on the library's own copy streams while chunk k runs
  * on `stream`, the state passing between chunks as in srwm_forward_from.  Results equal srwm_forward's within fp32 rounding (a
  * chunk restarts its first read-out from the stored state).
@@ -327,12 +329,12 @@ int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long 
 
 /*
  * srwm_debug_chunk_plan -- tests only: the chunk lengths srwm_forward_host
- * uses for T steps and the given chunk_steps, in order, into out (room for
+ * uses for T steps of width d and the given chunk_steps, in order, into out (room for
  * max_chunks, caller-owned).  Returns the number of chunks (which may exceed
  * max_chunks; only the first max_chunks are written), or -1 for T < 0,
  * max_chunks < 0, or out NULL with max_chunks > 0.
  */
-int srwm_debug_chunk_plan(int T, int chunk_steps, int* out, int max_chunks);
+int srwm_debug_chunk_plan(int T, int d, int chunk_steps, int* out, int max_chunks);
 
 /*
  * srwm_debug_set_segment_len -- tests only: force the segment length (a

@@ -64,7 +64,7 @@ def _lib():
         lib.srwm_debug_wrap_len.restype = LL
         lib.srwm_debug_wrap_pieces.argtypes = [LL, I, LL, LL, P, I]
         lib.srwm_debug_wrap_pieces.restype = I
-        lib.srwm_debug_chunk_plan.argtypes = [I, I, P, I]
+        lib.srwm_debug_chunk_plan.argtypes = [I, I, I, P, I]
         lib.srwm_debug_chunk_plan.restype = I
         lib.srwm_forward_from.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         lib.srwm_forward_from.restype = I
@@ -208,14 +208,14 @@ def srwm_debug_wrap_pieces(n_streams: int, T: int, wrap_len: int, slot: int):
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
 
-def srwm_debug_chunk_plan(T: int, chunk_steps: int = 0):
-    """The chunk lengths srwm_forward_host uses for T steps."""
+def srwm_debug_chunk_plan(T: int, d: int = 64, chunk_steps: int = 0):
+    """The chunk lengths srwm_forward_host uses for T steps of width d."""
     lib = _lib()
-    n = lib.srwm_debug_chunk_plan(int(T), int(chunk_steps), None, 0)
+    n = lib.srwm_debug_chunk_plan(int(T), int(d), int(chunk_steps), None, 0)
     if n < 0:
         raise SrwmError(SRWM_ERR_SHAPE, "srwm_debug_chunk_plan")
     buf = (ctypes.c_int * max(n, 1))()
-    lib.srwm_debug_chunk_plan(int(T), int(chunk_steps), buf, n)
+    lib.srwm_debug_chunk_plan(int(T), int(d), int(chunk_steps), buf, n)
     return list(buf[:n])
 
 

@@ -407,11 +407,18 @@ bool host_ws(long long B, long long T, long long H, long long d, long long n_lr,
 }
 
 // Chunk plan of srwm_forward_host.  chunk_steps > 0: chunks of that many steps
-// (the last one ragged).  0: chunks that double from 32 steps up to 256 (or
-// T / 8 for longer sequences) and halve again at the end, the middle split
-// evenly, so that the first input copy and the last output copy (which
-// nothing overlaps) stay short while there are few launches.
-std::vector<int> chunk_plan(int T, int chunk_steps)
+// (the last one ragged).  0: chunks that double from 32 steps and halve again
+// at the end, the middle split evenly, so that the first input copy and the
+// last output copy (which nothing overlaps) stay short.  The longest chunk
+// depends on which side sets the pace.  A step copies 8 d bytes per stream
+// each way and does 3 m d FMAs, i.e. 3 m / 8 FMAs per copied byte: ~37 at
+// d = 32, ~20 at d = 16, 73.5 at d = 64.  At d <= 32 the host link (~0.3 TB/s
+// both ways) is slower than the recurrence, and short chunks (at most 64
+// steps) keep the copies flowing from the start (rl: 1.24 ms per call against
+// 1.35 ms with 160-step chunks); at d = 64 the recurrence is the slower side,
+// and chunks of up to 256 steps, or T / 8 for longer sequences, save launches
+// and state reloads.
+std::vector<int> chunk_plan(int T, int d, int chunk_steps)
 {
     std::vector<int> plan;
     if (T <= 0) return plan;
@@ -420,7 +427,7 @@ std::vector<int> chunk_plan(int T, int chunk_steps)
         return plan;
     }
     constexpr int kMin = 32;
-    const int kMax = T / 8 > 256 ? T / 8 : 256;
+    const int kMax = d <= 32 ? 64 : (T / 8 > 256 ? T / 8 : 256);
     std::vector<int> tail;
     int rem = T;
     // A ramp chunk goes on both ends while at least as much is left between
@@ -440,10 +447,10 @@ std::vector<int> chunk_plan(int T, int chunk_steps)
     return plan;
 }
 
-int effective_chunk(int T, int chunk_steps)
+int effective_chunk(int T, int d, int chunk_steps)
 {
     int c = 1;
-    for (int v : chunk_plan(T, chunk_steps)) c = v > c ? v : c;
+    for (int v : chunk_plan(T, d, chunk_steps)) c = v > c ? v : c;
     return c;
 }
 
@@ -517,10 +524,10 @@ int srwm_debug_wrap_pieces(long long n_streams, int T, long long wrap_len, long 
     return n;
 }
 
-int srwm_debug_chunk_plan(int T, int chunk_steps, int* out, int max_chunks)
+int srwm_debug_chunk_plan(int T, int d, int chunk_steps, int* out, int max_chunks)
 {
     if (T < 0 || max_chunks < 0 || (max_chunks > 0 && !out)) return -1;
-    const std::vector<int> plan = chunk_plan(T, chunk_steps);
+    const std::vector<int> plan = chunk_plan(T, d, chunk_steps);
     for (int i = 0; i < static_cast<int>(plan.size()) && i < max_chunks; ++i) out[i] = plan[i];
     return static_cast<int>(plan.size());
 }
@@ -692,7 +699,7 @@ size_t srwm_forward_host_workspace_bytes(int B, int T, int H, int d, int n_lr, i
 {
     if (check_params(B, T, H, d, n_lr, 0) != SRWM_OK) return 0;
     HostWs w;
-    host_ws(B, T, H, d, n_lr, effective_chunk(T, chunk_steps), &w);
+    host_ws(B, T, H, d, n_lr, effective_chunk(T, d, chunk_steps), &w);
     return w.total;
 }
 
@@ -703,7 +710,7 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
     if (!W0_host || !W_final_host || !workspace || (T > 0 && (!x_host || !y_host))) return SRWM_ERR_NULL;
     int rc = check_params(B, T, H, d, n_lr, softmax_input);
     if (rc != SRWM_OK) return rc;
-    const int C = effective_chunk(T, chunk_steps);
+    const int C = effective_chunk(T, d, chunk_steps);
     HostWs w;
     host_ws(B, T, H, d, n_lr, C, &w);
     if (workspace_bytes < w.total) return SRWM_ERR_SHAPE;
@@ -742,7 +749,7 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
     if (T == 0) {
         if ((rc = run(nullptr, W0d, 0, B, 0, H, d, n_lr, softmax_input, nullptr, S, sc)) != SRWM_OK) return rc;
     }
-    const std::vector<int> plan = chunk_plan(T, chunk_steps);
+    const std::vector<int> plan = chunk_plan(T, d, chunk_steps);
     const int K = static_cast<int>(plan.size());
     for (int k = 0, t0 = 0; k < K; t0 += plan[k], ++k) {
         const int slot = k % kPipeSlots, Ck = plan[k];

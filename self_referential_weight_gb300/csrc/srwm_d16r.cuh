@@ -12,7 +12,8 @@
 // row 32 + l (a q row for l < 16, beta row l - 16 for 16 <= l < 16 + n_lr,
 // nothing above).  So the dot products of every row finish inside its lane,
 // the k entries of z sit in the upper half-warp and the q entries in the
-// lower half, and each softmax is a 16-lane butterfly within its half.
+// lower half, and both softmaxes take whole-warp redux.sync reductions with
+// the other half masked out.
 // u = phi(q) - phi(k) takes one cross-half shuffle; u, phi(k) and x~ reach
 // every lane as broadcast shared-memory reads.  Only s = phi(k_t) . x~_{t+1}
 // is summed over the warp.
@@ -47,17 +48,21 @@ __device__ __forceinline__ float2 pair_lo(float4 v) { return make_float2(v.x, v.
 __device__ __forceinline__ float2 pair_hi(float4 v) { return make_float2(v.z, v.w); }
 
 // softmax over the 16 values of each half-warp (lane l holds entry l % 16 of
-// its half); xor butterflies inside the half, so every lane of a half ends
-// with the same maximum and sum bits.
+// its half).  Whole-warp reductions with the other half masked out: the
+// maximum by redux.sync.max, the sum of the exponentials exactly in fixed
+// point (2^-27 steps, so sixteen values in [0, 1] fit 32 bits) by
+// redux.sync.add.  Every lane of a half ends with the same shift and sum bits.
 __device__ __forceinline__ float softmax16(float v)
 {
-    float mx = v;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float e = __expf(v - mx);
-    float sum = e;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const bool lo = (threadIdx.x & 16) == 0;
+    const float ninf = __int_as_float(0xff800000);
+    const float m_lo = redux_max(lo ? v : ninf);
+    const float m_hi = redux_max(lo ? ninf : v);
+    const float e = __expf(v - (lo ? m_lo : m_hi));
+    const uint32_t q = __float2uint_rn(e * 134217728.0f);
+    const uint32_t s_lo = redux_add(lo ? q : 0u);
+    const uint32_t s_hi = redux_add(lo ? 0u : q);
+    const float sum = static_cast<float>(lo ? s_lo : s_hi) * 7.450580596923828125e-09f;
     return e * rcp_approx(sum);
 }
 

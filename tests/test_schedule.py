@@ -92,18 +92,25 @@ def test_wrap_pieces_invalid_arguments():
 
 # ---------------------------------------------------------------- host pipeline chunk plan
 
+def longest_chunk(T, d):
+    """Where the recurrence sets the pace (d = 64) chunks grow to 256 steps, or
+    T / 8 for longer sequences; where the host copies do (d <= 32), to 64."""
+    return 64 if d <= 32 else max(256, T // 8)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
 @pytest.mark.parametrize("T", [0, 1, 31, 63, 64, 65, 75, 95, 96, 200, 512, 1024, 1500, 2056, 8192])
-def test_chunk_plan_doubling(T):
-    """chunk_steps <= 0: chunks double from 32 steps up to at most half of
-    max(256, T / 8) and halve again at the end, the middle split evenly into
-    chunks of at most max(256, T / 8); they cover the T steps in order.  Short
+def test_chunk_plan_doubling(T, d):
+    """chunk_steps <= 0: chunks double from 32 steps up to at most half the
+    longest chunk and halve again at the end, the middle split evenly into
+    chunks of at most the longest; they cover the T steps in order.  Short
     first and last chunks keep the copies that nothing overlaps short."""
-    plan = binding.srwm_debug_chunk_plan(T, 0)
+    plan = binding.srwm_debug_chunk_plan(T, d, 0)
     assert sum(plan) == T and all(c > 0 for c in plan)
     if T == 0:
         assert plan == []
         return
-    assert max(plan) <= max(256, T // 8)
+    assert max(plan) <= longest_chunk(T, d)
     ramp = 0
     while ramp < len(plan) // 2 and plan[ramp] == 32 << ramp and plan[-1 - ramp] == 32 << ramp:
         ramp += 1
@@ -111,16 +118,23 @@ def test_chunk_plan_doubling(T):
     assert not mid or max(mid) - min(mid) <= 1   # the middle split evenly
     if T >= 96:   # room for a 32-step chunk at both ends and as much between them
         assert plan[0] == 32 and plan[-1] == 32
-    else:
-        assert plan == [T]
+    else:         # no ramp: T split evenly into as few chunks as the longest allows
+        assert len(plan) == -(-T // longest_chunk(T, d)) and max(plan) - min(plan) <= 1
 
 
-def test_chunk_plan_rises_then_falls():
+def test_chunk_plan_by_width():
+    assert binding.srwm_debug_chunk_plan(512, 32, 0) == [32] + [64] * 7 + [32]          # rl
+    assert binding.srwm_debug_chunk_plan(1024, 64, 0) == [32, 64, 128, 192, 192, 192, 128, 64, 32]   # mid
+    assert binding.srwm_debug_chunk_plan(26, 16, 0) == [26]                              # few-shot
+
+
+@pytest.mark.parametrize("d", [16, 64])
+def test_chunk_plan_rises_then_falls(d):
     """chunk_steps <= 0: over every length up to 4,096 steps (and some longer
     ones) the chunks never shrink and then grow again, so a chunk whose copies
     nothing overlaps is never in the middle of the call."""
     for T in list(range(1, 4097)) + [6000, 8192, 10000, 65536]:
-        plan = binding.srwm_debug_chunk_plan(T, 0)
+        plan = binding.srwm_debug_chunk_plan(T, d, 0)
         assert sum(plan) == T
         top = plan.index(max(plan))
         assert all(a <= b for a, b in zip(plan[:top], plan[1:top + 1])), (T, plan)
@@ -129,5 +143,5 @@ def test_chunk_plan_rises_then_falls():
 
 @pytest.mark.parametrize("T,c", [(75, 32), (64, 64), (100, 1), (5, 128)])
 def test_chunk_plan_fixed(T, c):
-    plan = binding.srwm_debug_chunk_plan(T, c)
+    plan = binding.srwm_debug_chunk_plan(T, 64, c)
     assert sum(plan) == T and all(v == c for v in plan[:-1]) and 0 < plan[-1] <= c
