@@ -6,7 +6,10 @@ section 2.3, Eqs. (1)-(5)):
   * with the input softmax, beta rows of -60: every gate sigma(-60) ~ 9e-27,
     so W_final = W0 bit for bit and again y_t = W0^y x~_t;
   * saturating inputs (x scaled by 5 and 25): near one-hot softmaxes, against
-    the oracle within a few times the problem's own fp32 floor.
+    the oracle within a few times the problem's own fp32 floor;
+  * uniform softmaxes (all k rows of W0 equal, and constant x on some steps
+    with the input softmax): the kernels' fixed-point sums of exponentials
+    reach their largest value, d terms of exactly 1.
 """
 import numpy as np
 import pytest
@@ -66,7 +69,7 @@ def test_closed_gates_keep_W0(d, n_lr):
     assert rel(y, y_rows_matmul(x, W0, True)) <= 1e-5
 
 
-@pytest.mark.parametrize("d,n_lr,smx", [(16, 4, False), (32, 1, False), (64, 4, False), (64, 1, True)])
+@pytest.mark.parametrize("d,n_lr,smx", [(16, 4, False), (16, 1, True), (32, 1, False), (64, 4, False), (64, 1, True)])
 @pytest.mark.parametrize("scale", [5.0, 25.0])
 def test_saturating_inputs(d, n_lr, smx, scale):
     """Inputs scaled up drive the softmaxes towards one-hot, where the
@@ -81,3 +84,25 @@ def test_saturating_inputs(d, n_lr, smx, scale):
     y32, W32 = oracle.forward(x, W0, n_lr, smx, precision="f32")
     assert rel(y, yo) <= max(1e-4, 4 * rel(y32, yo))
     assert rel(Wf, Wo) <= max(1e-4, 4 * rel(W32, Wo))
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("smx", [False, True])
+def test_uniform_softmaxes(d, smx):
+    """All k rows of W0 equal: equal rows get equal updates (same block, same
+    gate, same a), so k_t has d equal entries at every step and phi(k_t) is
+    exactly uniform; every exponential is 1 and the fixed-point sums reach
+    their largest value (at d = 16, 16 * 2^27 = 2^31).  With the input softmax,
+    every seventh step's x is constant, so x~ is uniform there too.  Against
+    the oracle at the parity bar."""
+    wl = inputs.Workload("t", 3, 70, 2, d, 4, smx, 90 + d, "normal")
+    x, W0 = inputs.make_inputs(wl)
+    W0, x = W0.copy(), x.copy()
+    W0[:, d:2 * d] = W0[:, d:d + 1]
+    if smx:
+        x[:, ::7] = 0.5
+    y, Wf = run(x, W0, 4, smx)
+    assert np.all(Wf[:, :, d:2 * d] == Wf[:, :, d:d + 1])   # the k rows stay equal
+    yo, Wo = oracle.forward(x, W0, 4, smx)
+    assert rel(y, yo) <= 1e-4
+    assert rel(Wf, Wo) <= 1e-4
