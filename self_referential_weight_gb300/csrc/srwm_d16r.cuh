@@ -15,8 +15,9 @@
 // lower half, and both softmaxes take whole-warp redux.sync reductions with
 // the other half masked out.
 // u = phi(q) - phi(k) takes one cross-half shuffle; u, phi(k) and x~ reach
-// every lane as broadcast shared-memory reads.  Only s = phi(k_t) . x~_{t+1}
-// is summed over the warp.
+// every lane as broadcast shared-memory reads, and every lane forms
+// s = phi(k_t) . x~_{t+1} itself in the pass over W, so no sum over the warp
+// is left in the step.
 //
 // One step t, on W_{t-1} in registers:
 //   a_r       = W[r,:] . u_t                  (Eq. (2))
@@ -295,20 +296,18 @@ __global__ void __launch_bounds__(d16::Cfg<NLR, SMX>::NT, 2)
                 float g[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) g[r] = __shfl_sync(0xffffffffu, sg, 16 + (NLR == 1 ? 0 : r));
-                if (lo_half) {
-                    sm.pk[ps][lane] = pk;
-                    sm.u[t & 1][lane] = u;
-                }
-                // s = phi(k_t) . x~_{t+1}: each entry once (lower half), summed over the warp
-                float s = lo_half ? pk * xrow[col] : 0.f;
+                // both halves hold phi(k)[col] and u[col]: every lane stores (the
+                // upper half repeats the lower half's values), no divergence
+                sm.pk[ps][col] = pk;
+                sm.u[t & 1][col] = u;
                 __syncwarp();
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 // one pass over W: the pending update of step t - 1 (Eq. (3)),
-                // then a = W u_t and b = W x~_{t+1} on the updated columns
+                // then a = W u_t and b = W x~_{t+1} on the updated columns, and
+                // s = phi(k_t) . x~_{t+1} beside them (every lane, the same bits)
                 const float* pkp = sm.pk[pp];
                 const float* un = sm.u[t & 1];
-                float2 cc[2], aa[2], bb[2];
+                const float* pkc = sm.pk[ps];
+                float2 cc[2], aa[2], bb[2], ss = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     cc[i] = make_float2(coef[i], coef[i]);
@@ -319,6 +318,9 @@ __global__ void __launch_bounds__(d16::Cfg<NLR, SMX>::NT, 2)
                     const float4 p4 = lds4(pkp + 4 * j);
                     const float4 u4 = lds4(un + 4 * j);
                     const float4 x4 = lds4(xrow + 4 * j);
+                    const float4 k4 = lds4(pkc + 4 * j);
+                    ss = __ffma2_rn(pair_lo(k4), pair_lo(x4), ss);
+                    ss = __ffma2_rn(pair_hi(k4), pair_hi(x4), ss);
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         w[i][2 * j] = __ffma2_rn(cc[i], pair_lo(p4), w[i][2 * j]);
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(d16::Cfg<NLR, SMX>::NT, 2)
                         bb[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(x4), bb[i]);
                     }
                 }
+                const float s = ss.x + ss.y;
                 const float a0 = aa[0].x + aa[0].y, a1 = aa[1].x + aa[1].y;
                 const float ga = blk_a == 0 ? g[0] : g[1];
                 const float gb = blk_b == 0 ? g[0] : (blk_b == 2 ? g[2] : g[3]);
