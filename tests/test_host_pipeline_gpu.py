@@ -87,11 +87,13 @@ def test_host_pipeline_rejects_device_memory():
     assert rc == 3
 
 
-@pytest.mark.parametrize("T", [1, 63, 64, 200, 700])
-def test_host_pipeline_doubling_plan(T):
-    """The default chunk plan (doubling from 32 steps, halving at the end) over
-    several lengths equals srwm_forward within fp32 rounding."""
-    wl = inputs.Workload("t", 2, T, 2, 32, 1, True, 900 + T, "normal")
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("T", [1, 63, 64, 95, 200, 700, 2056])
+def test_host_pipeline_doubling_plan(T, d):
+    """The default chunk plan (doubling from 32 steps, an even middle whose
+    longest chunk depends on d, halving at the end) over several lengths
+    equals srwm_forward within fp32 rounding."""
+    wl = inputs.Workload("t", 2, T, 2, d, 1, True, 900 + T + d, "normal")
     x, W0 = inputs.make_inputs(wl)
     y, Wf = host_forward(x, W0, 1, True, 0)
     yd, Wd = binding.srwm_forward(torch.from_numpy(x).to(DEV), torch.from_numpy(W0).to(DEV), 1, True)
