@@ -113,6 +113,13 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
     const float q0 = zt[2 * D + lane], q1 = zt[2 * D + 32 + lane];
     const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
 
+    // the softmaxes first in source order: their long-latency reductions are
+    // then issued ahead of the update's FMAs, which fill the waits (measured
+    // 1.7 % faster on the long workload than the reverse order)
+    float pk0, pk1, pq0, pq1;
+    softmax64(k0, k1, pk0, pk1);
+    softmax64(q0, q1, pq0, pq1);
+
     float2 x2[NP];
     load_pairs(xn, cg, x2);
     float2 accb[NS];
@@ -126,10 +133,6 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
             accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
         }
     }
-
-    float pk0, pk1, pq0, pq1;
-    softmax64(k0, k1, pk0, pk1);
-    softmax64(q0, q1, pq0, pq1);
     float g[4];
     if constexpr (NLR == 4) {
         g[0] = sigmoid_fast(beta.x);
