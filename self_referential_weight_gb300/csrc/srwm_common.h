@@ -14,6 +14,9 @@ SRWM_HD constexpr int rup(int a, int b) { return cdiv(a, b) * b; }
 
 // Bits of the device status word.
 constexpr unsigned kStatusTimeout = 1u;
+// The dynamic shared memory base was not 128-byte aligned (the kernels place
+// TMA buffers at 128-byte offsets from it); the kernel did nothing.
+constexpr unsigned kStatusSmemBase = 2u;
 
 // Kernel arguments besides the two tensor maps.
 struct KParams {

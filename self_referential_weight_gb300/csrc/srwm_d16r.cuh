@@ -99,10 +99,10 @@ __global__ void __launch_bounds__(d16::Cfg<NLR, SMX>::NT, 2)
     using d16::pair_hi;
     using d16::pair_lo;
     constexpr int D = C::D, TAU = C::TAU, NP = C::NP;
-    extern __shared__ unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    d16::Smem<C>& sm = reinterpret_cast<d16::Smem<C>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127))[warp];
+    d16::Smem<C>& sm = reinterpret_cast<d16::Smem<C>*>(smem_raw)[warp];
+    if (!smem_base_ok(smem_raw, kp.status)) return;
     constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
 
     const bool lo_half = lane < 16;               // rows y (A) and q (B); else k (A) and beta (B)

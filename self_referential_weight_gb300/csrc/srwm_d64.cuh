@@ -234,8 +234,9 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     constexpr int M = 3 * D + NLR;
     constexpr int S1 = SLOTS + 1;
     constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
-    extern __shared__ unsigned char smem_raw[];
-    Smem<NW>& sm = *reinterpret_cast<Smem<NW>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem<NW>& sm = *reinterpret_cast<Smem<NW>*>(smem_raw);
+    if (!smem_base_ok(smem_raw, kp.status)) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 2, cg = tid & 3;

@@ -100,15 +100,51 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, const KParams& kp, int
     float* u_cur = sm.u[warp];
     const int bc = 4 * (tid & 15);   // beta columns of this thread
 
-    // ---- 1. softmaxes (every warp, all 64 entries), phi_k and u
+    // ---- 1. the softmaxes (every warp, all 64 entries: the step's chain)
+    // beside the pending update of step t - 1 and b = W_{t-1} x~_{t+1}, which
+    // do not depend on them
     float pk0, pk1, pq0, pq1;
     softmax64(zt[D + lane], zt[D + 32 + lane], pk0, pk1);
     softmax64(zt[2 * D + lane], zt[2 * D + 32 + lane], pq0, pq1);
+
+    float2 bb[3];
+    {
+        float2 cc[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            cc[i] = make_float2(coef[i], coef[i]);
+            bb[i] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j) {
+            const float4 p4 = lds4(pk_prev + 4 * j);
+            const float4 x4 = lds4(xn + 4 * j);
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                w[i][2 * j] = __ffma2_rn(cc[i], pair_lo(p4), w[i][2 * j]);
+                w[i][2 * j + 1] = __ffma2_rn(cc[i], pair_hi(p4), w[i][2 * j + 1]);
+                bb[i] = __ffma2_rn(w[i][2 * j], pair_lo(x4), bb[i]);
+                bb[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(x4), bb[i]);
+            }
+        }
+    }
+    float bbb;
+    {
+        const float4 p4 = lds4(pk_prev + bc);
+        wb.x = fmaf(coefb, p4.x, wb.x);
+        wb.y = fmaf(coefb, p4.y, wb.y);
+        wb.z = fmaf(coefb, p4.z, wb.z);
+        wb.w = fmaf(coefb, p4.w, wb.w);
+        const float4 x4 = lds4(xn + bc);
+        bbb = fmaf(wb.x, x4.x, fmaf(wb.y, x4.y, fmaf(wb.z, x4.z, wb.w * x4.w)));
+    }
+
+    // ---- 2. phi_k and u = phi(q) - phi(k) to the warp's buffers.  u takes an
+    // explicit rounded subtraction: a contracted fma(e_q, 1/sum_q, -phi(k))
+    // would skip phi(q)'s rounding, so equal k and q rows would no longer give
+    // u = 0 exactly
     pk_cur[lane] = pk0;
     pk_cur[lane + 32] = pk1;
-    // u = phi(q) - phi(k) with an explicit rounded subtraction: a contracted
-    // fma(e_q, 1/sum_q, -phi(k)) would skip phi(q)'s rounding, so equal k and
-    // q rows would no longer give u = 0 exactly
     u_cur[lane] = __fsub_rn(pq0, pk0);
     u_cur[lane + 32] = __fsub_rn(pq1, pk1);
     // backward record of step t: phi(k), u, gates, a (the rows' a follow below)
@@ -123,54 +159,34 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, const KParams& kp, int
         }
     }
     const float sp = fmaf(pk0, xn[lane], pk1 * xn[lane + 32]);
-    const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
     __syncwarp();
-    // ---- 2. s and the beta rows
+
+    // ---- 3. a = W_{t-1} u (the chain), s and the beta rows' sums beside it
     const float s = warp_allsum(sp);
-    float abb, bbb;
+    float abb;
     {
-        const float4 p4 = lds4(pk_prev + bc);
-        wb.x = fmaf(coefb, p4.x, wb.x);
-        wb.y = fmaf(coefb, p4.y, wb.y);
-        wb.z = fmaf(coefb, p4.z, wb.z);
-        wb.w = fmaf(coefb, p4.w, wb.w);
         const float4 u4 = lds4(u_cur + bc);
-        const float4 x4 = lds4(xn + bc);
         abb = fmaf(wb.x, u4.x, fmaf(wb.y, u4.y, fmaf(wb.z, u4.z, wb.w * u4.w)));
-        bbb = fmaf(wb.x, x4.x, fmaf(wb.y, x4.y, fmaf(wb.z, x4.z, wb.w * x4.w)));
     }
 #pragma unroll
     for (int o = 1; o <= 8; o <<= 1) {
         abb += __shfl_xor_sync(0xffffffffu, abb, o);
         bbb += __shfl_xor_sync(0xffffffffu, bbb, o);
     }
-
-    // ---- 3. one pass over W: pending update, then a = W u and b = W x~_{t+1}
-    float2 aa[3], bb[3];
-    {
-        float2 cc[3];
+    float2 aa[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) aa[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NP / 2; ++j) {
+        const float4 u4 = lds4(u_cur + 4 * j);
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
-            cc[i] = make_float2(coef[i], coef[i]);
-            aa[i] = bb[i] = make_float2(0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < NP / 2; ++j) {
-            const float4 p4 = lds4(pk_prev + 4 * j);
-            const float4 u4 = lds4(u_cur + 4 * j);
-            const float4 x4 = lds4(xn + 4 * j);
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                w[i][2 * j] = __ffma2_rn(cc[i], pair_lo(p4), w[i][2 * j]);
-                w[i][2 * j + 1] = __ffma2_rn(cc[i], pair_hi(p4), w[i][2 * j + 1]);
-                aa[i] = __ffma2_rn(w[i][2 * j], pair_lo(u4), aa[i]);
-                bb[i] = __ffma2_rn(w[i][2 * j], pair_lo(x4), bb[i]);
-                aa[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(u4), aa[i]);
-                bb[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(x4), bb[i]);
-            }
+            aa[i] = __ffma2_rn(w[i][2 * j], pair_lo(u4), aa[i]);
+            aa[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(u4), aa[i]);
         }
     }
     // ---- 4. gates and z_{t+1}
+    const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
     float g[4];
     if constexpr (NLR == 4) {
         g[0] = sigmoid_fast(beta.x);
@@ -208,8 +224,9 @@ __global__ void __launch_bounds__(d64r::NT, 4)
     using namespace d64r;
     constexpr int M = 3 * D + NLR;
     constexpr uint32_t kChunkBytes = TAU * D * sizeof(float);
-    extern __shared__ unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    if (!smem_base_ok(smem_raw, kp.status)) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int br = tid >> 4, bc = 4 * (tid & 15);   // this thread's beta row and columns

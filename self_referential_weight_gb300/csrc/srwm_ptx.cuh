@@ -5,11 +5,24 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "srwm_common.h"
+
 namespace srwm {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// The kernels lay their shared-memory structures out from the dynamic shared
+// memory base, which they take to be 128-byte aligned (TMA buffers sit at
+// 128-byte offsets from it).  Checked once at entry: on a misaligned base the
+// CTA reports it in the status word and returns before touching anything.
+__device__ __forceinline__ bool smem_base_ok(const void* base, unsigned* status)
+{
+    if ((smem_u32(base) & 127u) == 0) return true;
+    if (threadIdx.x == 0) atomicOr(status, kStatusSmemBase);
+    return false;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns()
