@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the device timing of the other workloads (long, rl, fewshot) on one GPU")
     ap.add_argument("--backward", action="store_true",
                     help="time srwm_backward (gradients of a loss on y) on the workload instead; prints its own line")
     ap.add_argument("--layer", action="store_true",
@@ -184,6 +186,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def cpu_model():
+    """The host CPU's vendor and model as lscpu or /proc/cpuinfo report them."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        info = {}
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            info.setdefault(k.strip(), v.strip())
+        parts = [info.get("Vendor ID"), info.get("Model name")]
+        if any(parts):
+            return " ".join(p for p in parts if p)
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.partition(":")[2].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl, x, W0, target_s=10.0):
     """The float64 oracle, as it stands, on this host's cores, on a bounded sample
     of the workload's (b, h) streams at full T.  Returns the JSON object."""
@@ -194,12 +219,12 @@ def cpu_baseline(wl, x, W0, target_s=10.0):
     n_cal = min(wl.B * wl.H, max(cores, 8))
     pairs = [(i // wl.H, i % wl.H) for i in range(wl.B * wl.H)]
 
-    def run(n):
+    def run(n, threads=cores):
         sel = pairs[:n]
         xs = np.ascontiguousarray(np.stack([x[b, :, h] for b, h in sel], axis=0)[:, :, None, :])
         Ws = np.ascontiguousarray(np.stack([W0[h] for _, h in sel], axis=0)[:, None])
         t0 = time.perf_counter()
-        oracle.forward(xs, Ws, wl.n_lr, wl.softmax_input, per_sequence=True, n_threads=cores)
+        oracle.forward(xs, Ws, wl.n_lr, wl.softmax_input, per_sequence=True, n_threads=threads)
         return time.perf_counter() - t0
 
     t_cal = run(n_cal)
@@ -207,10 +232,16 @@ def cpu_baseline(wl, x, W0, target_s=10.0):
     n = max(cores, (n // cores) * cores) if n >= cores else n
     n = min(n, wl.B * wl.H)
     dt = run(n)
+    # the same oracle on one core, on a sample of ~3 s
+    n1 = max(1, min(wl.B * wl.H, int(3.0 * n_cal / max(t_cal * cores, 1e-6))))
+    dt1 = run(n1, threads=1)
     return {"value": n * wl.T / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {wl.B * wl.H} (b,h) streams x {wl.T} steps of the {wl.name} "
                       f"workload, float64 C oracle, one pthread per core over streams",
-            "seconds": dt}
+            "seconds": dt,
+            "one_core": {"value": n1 * wl.T / dt1, "unit": UNIT, "cores": 1,
+                         "sample": f"{n1} streams x {wl.T} steps, one thread", "seconds": dt1},
+            "cpu_model": cpu_model()}
 
 
 def reference_arm(args, wl):
@@ -430,6 +461,16 @@ def main():
         "ms_per_step_best": min(per_step),
         "ms_per_step_median": statistics.median(per_step),
     }
+    if world == 1 and not args.no_extra:
+        # the other workloads, each timed on the device the same way; the
+        # headline value and config stay the workload above
+        del x, W0, y, Wf
+        torch.cuda.empty_cache()
+        extra_steps = max(10, min(args.steps, 50))
+        line["other_workloads"] = {
+            name: time_other_workload(binding, name, extra_steps, args.warmup, dev, flush, not args.no_clocks, n_sm,
+                                      peak_tflops)
+            for name in ("mid", "long", "rl", "fewshot") if name != wl.name}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, x_np, W0_np)
     print(json.dumps(line), flush=True)
@@ -437,6 +478,56 @@ def main():
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def time_other_workload(binding, name, steps, warmup, dev, flush, sample_clocks, n_sm, peak_tflops):
+    """Device time of srwm_forward_balanced on another workload (one GPU):
+    K timed calls after W warm-ups, L2 flushed between calls, CUDA events on
+    the launching stream, clocks sampled during the timed region."""
+    import torch
+
+    wl = inputs.workload(name)
+    x_np, W0_np = inputs.make_inputs(wl)
+    x, W0 = torch.from_numpy(x_np).to(dev), torch.from_numpy(W0_np).to(dev)
+    y = torch.empty_like(x)
+    Wf = torch.empty((wl.B, wl.H, wl.m, wl.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.srwm_forward_workspace_bytes(wl.B, wl.H), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.srwm_forward_balanced(x, W0, wl.n_lr, wl.softmax_input, y_out=y, W_final=Wf, workspace=ws,
+                                      stream=stream)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    with (clocks if sample_clocks else _Null()):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if binding.srwm_last_device_status(stream) != 0:
+        raise RuntimeError(f"device status set while timing {name}")
+    per_step = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = statistics.fmean(per_step)
+    flops = 2.0 * fmas_per_head_token(wl) * wl.head_tokens
+    achieved = flops / (ms / 1e3) / 1e12
+    kernel = kernel_name(wl, n_sm)
+    clk = clocks.summary() if sample_clocks else {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                                                  "samples": 0}
+    return {"config": workload_config(wl), "steps": steps, "ms_per_step": ms,
+            "ms_per_step_best": min(per_step), "ms_per_step_median": statistics.median(per_step),
+            "value": wl.head_tokens / (ms / 1e3), "unit": UNIT,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tflops, "traffic": profiled_traffic(kernel, wl.name),
+                         "kernel": kernel, "flops_per_launch": flops},
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]}}
 
 
 class _Null:

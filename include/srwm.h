@@ -21,8 +21,24 @@
  *
  * Common rules for every entry point below:
  *   - Pointers are DEVICE memory (cudaMalloc'd or managed) of fp32, contiguous,
- *     16-byte aligned.  The caller owns all buffers; the library allocates
- *     nothing and keeps no state except one device status word.
+ *     16-byte aligned.  The caller owns all buffers.  srwm_forward,
+ *     srwm_forward_balanced, srwm_forward_balanced_noalloc, srwm_forward_from,
+ *     srwm_step and srwm_backward make no device allocation.
+ *   - State the library keeps, per device, for the life of the process:
+ *       * the device status word (srwm_last_device_status), a file-scope
+ *         __device__ variable, present once the library is loaded; its device
+ *         address is looked up on the first call on each device;
+ *       * srwm_forward_balanced_noalloc's counter array (256 KiB), a
+ *         file-scope __device__ array, present once the library is loaded;
+ *         its address is looked up on that entry point's first call on each
+ *         device;
+ *       * srwm_forward_host's two copy streams and twelve events, created on
+ *         its first call on each device;
+ *       * srwm_layer_forward's cuBLASLt handle, created by cublasLtCreate
+ *         (which allocates) on its first call on each device.
+ *     The cached addresses and handles belong to the device's primary context:
+ *     after cudaDeviceReset on a device, do not call the library on that
+ *     device again in the same process.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without waiting.  Argument errors are
  *     returned before anything is enqueued; nothing is written then.

@@ -726,10 +726,6 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
         if (!hp) continue;
         if ((rc = check_host_ptr(hp)) != SRWM_OK) return rc;
     }
-    Pipe* pp = nullptr;
-    if ((rc = pipe_for_device(&pp)) != SRWM_OK) return rc;
-    Pipe& P = *pp;
-    std::lock_guard<std::mutex> lk(P.mu);
     cudaStream_t sc = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(workspace);
     float* W0d = reinterpret_cast<float*>(base + w.w0);
@@ -737,6 +733,38 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
     int* cnt = reinterpret_cast<int*>(base + w.cnt);
     const size_t row = static_cast<size_t>(H) * d * 4;   // one step of one sequence
     auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+    const std::vector<int> plan = chunk_plan(T, d, chunk_steps);
+    const int K = static_cast<int>(plan.size());
+
+    if (K <= 1) {
+        // One chunk (or none): there is nothing for the copies to overlap, so
+        // they run in order on the caller's stream, without the copy streams
+        // and the events that order them.
+        float* xb = reinterpret_cast<float*>(base + w.x[0]);
+        float* yb = reinterpret_cast<float*>(base + w.y[0]);
+        if (fail(cudaMemcpyAsync(W0d, W0_host, static_cast<size_t>(H * m * d) * 4, cudaMemcpyHostToDevice, sc)) ||
+            (T > 0 && fail(cudaMemcpyAsync(xb, x_host, nx, cudaMemcpyHostToDevice, sc)))) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        if (T == 0) {
+            if ((rc = run(nullptr, W0d, 0, B, 0, H, d, n_lr, softmax_input, nullptr, S, sc)) != SRWM_OK) return rc;
+        } else if ((rc = run(xb, W0d, 0, B, T, H, d, n_lr, softmax_input, yb, S, sc, cnt,
+                             static_cast<size_t>(B) * H * 4)) != SRWM_OK) {
+            return rc;
+        }
+        if ((T > 0 && fail(cudaMemcpyAsync(y_host, yb, nx, cudaMemcpyDeviceToHost, sc))) ||
+            fail(cudaMemcpyAsync(W_final_host, S, nwf, cudaMemcpyDeviceToHost, sc))) {
+            cudaGetLastError();
+            return SRWM_ERR_CUDA;
+        }
+        return SRWM_OK;
+    }
+
+    Pipe* pp = nullptr;
+    if ((rc = pipe_for_device(&pp)) != SRWM_OK) return rc;
+    Pipe& P = *pp;
+    std::lock_guard<std::mutex> lk(P.mu);
 
     // the copy streams start after the work already on the caller's stream
     if (fail(cudaEventRecord(P.start, sc)) || fail(cudaStreamWaitEvent(P.s_in, P.start, 0)) ||
@@ -746,11 +774,6 @@ int srwm_forward_host(const float* x_host, const float* W0_host, int B, int T, i
         cudaGetLastError();
         return SRWM_ERR_CUDA;
     }
-    if (T == 0) {
-        if ((rc = run(nullptr, W0d, 0, B, 0, H, d, n_lr, softmax_input, nullptr, S, sc)) != SRWM_OK) return rc;
-    }
-    const std::vector<int> plan = chunk_plan(T, d, chunk_steps);
-    const int K = static_cast<int>(plan.size());
     for (int k = 0, t0 = 0; k < K; t0 += plan[k], ++k) {
         const int slot = k % kPipeSlots, Ck = plan[k];
         float* xb = reinterpret_cast<float*>(base + w.x[slot]);

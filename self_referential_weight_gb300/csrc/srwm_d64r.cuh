@@ -19,16 +19,17 @@
 // so that W and little else stays in the 255 registers.
 //
 // One step:
-//   1. each warp reads k_t, q_t, beta_t (exchanged through shared memory at
-//      the previous barrier) and computes phi_k, phi_q over all 64 entries
-//      (two per lane), so both warps hold the same values without a second
-//      barrier; phi_k and u = phi_q - phi_k go to the warp's own buffers;
-//   2. s = phi_k . x~_{t+1} (a warp sum) and the beta rows' update and dots
-//      (sums over 16 lanes), issued ahead of the pass so that their shuffles
-//      overlap it;
-//   3. one pass over W: per float4 column chunk, the pending update of step
-//      t - 1, then a = W u and b = W x~_{t+1} on the updated columns, all with
-//      two-wide FMAs;
+//   1. each warp reads k_t, q_t (exchanged through shared memory at the
+//      previous barrier) and computes phi_k, phi_q over all 64 entries (two
+//      per lane), so both warps hold the same values without a second
+//      barrier.  Beside these softmaxes, which are the step's chain, the
+//      thread applies the pending update of step t - 1 to its rows and forms
+//      b = W_{t-1} x~_{t+1} (both independent of the softmaxes), per float4
+//      column chunk with two-wide FMAs; the beta rows likewise;
+//   2. phi_k and u = phi_q - phi_k go to the warp's own buffers (__syncwarp);
+//   3. a = W_{t-1} u for the thread's rows (two accumulators per row), with
+//      s = phi_k . x~_{t+1} (a warp sum) and the beta rows' sums over 16 lanes
+//      beside it;
 //   4. gates, the rows' z_{t+1} into shared memory (y rows into the TMA
 //      staging ring), barrier.
 // Steps run chunk by chunk: waits, TMA loads and stores sit at chunk
@@ -173,18 +174,23 @@ __device__ __forceinline__ void d64r_step(d64r::Smem& sm, const KParams& kp, int
         abb += __shfl_xor_sync(0xffffffffu, abb, o);
         bbb += __shfl_xor_sync(0xffffffffu, bbb, o);
     }
-    float2 aa[3];
+    // two accumulators per row (even and odd column chunks): six independent
+    // FMA chains instead of three
+    float2 aa[3], ao[3];
 #pragma unroll
-    for (int i = 0; i < 3; ++i) aa[i] = make_float2(0.f, 0.f);
+    for (int i = 0; i < 3; ++i) aa[i] = ao[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NP / 2; ++j) {
         const float4 u4 = lds4(u_cur + 4 * j);
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
-            aa[i] = __ffma2_rn(w[i][2 * j], pair_lo(u4), aa[i]);
-            aa[i] = __ffma2_rn(w[i][2 * j + 1], pair_hi(u4), aa[i]);
+            float2& acc = (j & 1) ? ao[i] : aa[i];
+            acc = __ffma2_rn(w[i][2 * j], pair_lo(u4), acc);
+            acc = __ffma2_rn(w[i][2 * j + 1], pair_hi(u4), acc);
         }
     }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) aa[i] = make_float2(aa[i].x + ao[i].x, aa[i].y + ao[i].y);
     // ---- 4. gates and z_{t+1}
     const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
     float g[4];

@@ -147,3 +147,29 @@ def test_backward_full_size_sampled_head(name, h):
     ox, oW = srwm_grad.grads(xs, W0[h:h + 1], wl.n_lr, wl.softmax_input, np.ascontiguousarray(dy[:, :, h:h + 1]))
     assert rel(dx[:, :, h:h + 1], ox) <= TOL, rel(dx[:, :, h:h + 1], ox)
     assert rel(dW0[h:h + 1], oW) <= TOL, rel(dW0[h:h + 1], oW)
+
+
+def test_backward_long_one_stream():
+    """The long workload (T = 8192, where recovering W_{t-1} by subtracting
+    each recorded update accumulates the most rounding) at full size through
+    srwm_backward, with dy zero on every stream but one.  The other streams'
+    gradients are then exactly zero, and dL/dW0[h] is that one stream's
+    contribution, which the oracle computes on the (b, h) slice alone.  The
+    bar is twice the forward's bound at this length (1e-3)."""
+    wl = inputs.workload("long")
+    b, h = 11, 6
+    x, W0 = inputs.make_inputs(wl)
+    dy, _ = inputs.make_cotangents(wl, False)
+    mask = np.zeros_like(dy)
+    mask[b, :, h] = 1.0
+    dy = dy * mask
+    dx, dW0 = run_bwd(x, W0, wl.n_lr, wl.softmax_input, dy, None)
+    ox, oW = srwm_grad.grads(np.ascontiguousarray(x[b:b + 1, :, h:h + 1]), W0[h:h + 1], wl.n_lr, wl.softmax_input,
+                             np.ascontiguousarray(dy[b:b + 1, :, h:h + 1]))
+    ex, ew = rel(dx[b:b + 1, :, h:h + 1], ox), rel(dW0[h:h + 1], oW)
+    print(f"long backward, stream ({b}, {h}): dx rel {ex:.2e}, dW0 rel {ew:.2e}")
+    assert ex <= 2e-3 and ew <= 2e-3, (ex, ew)
+    others = np.ones(dx.shape, bool)
+    others[b, :, h] = False
+    assert not dx[others].any()
+    assert not np.delete(dW0, h, axis=0).any()

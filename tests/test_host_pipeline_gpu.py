@@ -101,3 +101,17 @@ def test_host_pipeline_doubling_plan(T, d):
     yd, Wd = yd.cpu().numpy(), Wd.cpu().numpy()
     assert np.abs(y - yd).max() <= 1e-5 * np.abs(yd).max()
     assert np.abs(Wf - Wd).max() <= 1e-5 * np.abs(Wd).max()
+
+
+def test_host_pipeline_single_chunk_fewshot():
+    """The few-shot workload in full (T = 26: the default plan is one chunk,
+    which runs its copies in order on the caller's stream)."""
+    wl = inputs.workload("fewshot")
+    x, W0 = inputs.make_inputs(wl)
+    plan = binding.srwm_debug_chunk_plan(wl.T, wl.d, 0)
+    assert plan == [wl.T]
+    y, Wf = host_forward(x, W0, wl.n_lr, wl.softmax_input, 0)
+    yd, Wd = device_forward(x, W0, wl.n_lr, wl.softmax_input)
+    assert rel(y, yd) <= 1e-5 and rel(Wf, Wd) <= 1e-5
+    yo, Wo = oracle.forward(x, W0, wl.n_lr, wl.softmax_input)
+    assert rel(y, yo) <= 1e-4 and rel(Wf, Wo) <= 1e-4
