@@ -133,42 +133,65 @@ def profiled_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around a timed region.
+
+    Samples are read by a thread and time-stamped on arrival; entering waits
+    for the first sample, so sampling is running when the timed region starts.
+    summary(t0, t1) keeps the samples taken between t0 and t1 (wall clock),
+    which the caller brackets around the timed region plus a short roll of
+    the same work before and after it, so that a region of a few milliseconds
+    still gets samples under load."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.out = None
+        self.lines = []
+        self.thread = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line))
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t_end = time.time() + 5.0
+        while not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
-    def summary(self):
-        if not self.out:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    def summary(self, t0=None, t1=None):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+        for ts, line in list(self.lines):
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -184,6 +207,31 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+ROLL_S = 0.15   # seconds of untimed load on each side of a timed region while clocks are sampled
+
+
+def one_call_ms(step, stream):
+    """Device time of one call (for sizing the clock-sampling roll)."""
+    import torch
+
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def roll(step, seconds, ms_per_call):
+    """Runs `step` for about `seconds` of GPU time (untimed: it only keeps the
+    GPU under the same load while clocks are sampled around a timed region)."""
+    import torch
+
+    for _ in range(max(1, int(seconds * 1e3 / max(ms_per_call, 1e-3)))):
+        step()
+    torch.cuda.synchronize()
 
 
 def cpu_model():
@@ -341,22 +389,32 @@ def main():
     if binding.srwm_last_device_status(stream) != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # ---------------- device-timed region: K steps, L2 flushed between steps
+    est_ms = one_call_ms(step, stream)
+
+    # ---------------- device-timed region: K steps, L2 flushed between steps;
+    # clocks sampled over the region and a short roll of the same calls on
+    # either side of it
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
     with (clocks if not args.no_clocks else _Null()):
+        t_roll0 = time.time()
+        if not args.no_clocks:
+            roll(step, ROLL_S, est_ms)
+        barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
-    barrier()
-    t_wall = time.perf_counter() - t_wall
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+        if not args.no_clocks:
+            roll(step, ROLL_S, est_ms)
+        t_roll1 = time.time()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     t_dev = sum(per_step) / 1e3
     if binding.srwm_last_device_status(stream) != 0:
@@ -411,7 +469,7 @@ def main():
 
     if rank != 0:
         return
-    clk = clocks.summary() if not args.no_clocks else {"sm_mhz": None, "sm_max_mhz": None,
+    clk = clocks.summary(t_roll0, t_roll1) if not args.no_clocks else {"sm_mhz": None, "sm_max_mhz": None,
                                                         "reasons": ["unsampled"], "samples": 0}
     peaks = {}
     try:
@@ -454,7 +512,9 @@ def main():
         },
         "fma_probe": probe,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
-                   "reasons": clk["reasons"], "samples": clk["samples"]},
+                   "reasons": clk["reasons"], "samples": clk["samples"],
+                   "window": f"nvidia-smi every {ClockSampler.INTERVAL_MS} ms over the timed region and "
+                             f"{ROLL_S} s of the same calls on each side"},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "wall_s_timed_region": t_wall,
@@ -501,16 +561,23 @@ def time_other_workload(binding, name, steps, warmup, dev, flush, sample_clocks,
     for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
+    est_ms = one_call_ms(step, stream)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     clocks = ClockSampler(torch.cuda.current_device())
     with (clocks if sample_clocks else _Null()):
+        t_roll0 = time.time()
+        if sample_clocks:
+            roll(step, ROLL_S, est_ms)
         for i in range(steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        if sample_clocks:
+            roll(step, ROLL_S, est_ms)
+        t_roll1 = time.time()
     if binding.srwm_last_device_status(stream) != 0:
         raise RuntimeError(f"device status set while timing {name}")
     per_step = [a.elapsed_time(b) for a, b in zip(starts, ends)]
@@ -518,7 +585,8 @@ def time_other_workload(binding, name, steps, warmup, dev, flush, sample_clocks,
     flops = 2.0 * fmas_per_head_token(wl) * wl.head_tokens
     achieved = flops / (ms / 1e3) / 1e12
     kernel = kernel_name(wl, n_sm)
-    clk = clocks.summary() if sample_clocks else {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+    clk = clocks.summary(t_roll0, t_roll1) if sample_clocks else {"sm_mhz": None, "sm_max_mhz": None,
+                                                                  "reasons": ["unsampled"],
                                                   "samples": 0}
     return {"config": workload_config(wl), "steps": steps, "ms_per_step": ms,
             "ms_per_step_best": min(per_step), "ms_per_step_median": statistics.median(per_step),

@@ -70,12 +70,12 @@ struct Cfg {
 
 template <int NW>
 struct __align__(128) Smem {
-    float xring[2][TAU][D];    // TMA destination: raw x, two chunks
+    float xring[3][TAU][D];    // TMA destination: raw x, three chunks
     float ystage[3][TAU][D];   // TMA source: y, three chunks
     float z[2][D * 3 + 8];     // k, q, beta rows of z_t by step parity (index = row)
     float xs[2][D];            // x~_{t+1}, x~_{t+2}
     float pkq[NW][2][D];       // per warp: phi_k, phi_q in plain column order
-    uint64_t xbar[2];          // "chunk landed" barriers of the x ring
+    uint64_t xbar[3];          // "chunk landed" barriers of the x ring
 };
 
 __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&out)[NP])
@@ -90,49 +90,51 @@ __device__ __forceinline__ void load_pairs(const float* base, int cg, float2 (&o
 
 }  // namespace d64
 
+// The thread's state between steps, besides its W tile:
+//   coef[i]  g a of the pending update of step t-1 for slot i (the y slots'
+//            values are formed at the start of step t, see below);
+//   pkc      phi_k of step t-1 in the thread's column layout;
+//   u2       u of step t-1 in the column layout (for the y slots' a);
+//   yb       b of the two y slots for y_t (summed over the four column groups);
+//   ys, gy   s = phi_k . x~_t and the y block's gate, both of step t-1.
+template <int NW>
+struct D64Carry {
+    float2 pkc[d64::NP];
+    float2 u2[d64::NP];
+    float yb[2];
+    float ys, gy;
+};
+
 // One step of the recurrence for a warp whose threads carry NS row slots
-// (slots i < SLOTS: rows rg + RG i; slot SLOTS: beta row 192 + rg).  Reads z_t, phi
-// inputs and x~_{t+1} from shared memory, applies the pending update, writes
-// z_{t+1} (y rows to the staging buffer) and leaves this step's update pending
-// in (coef, pkc).
+// (slots i < SLOTS: rows rg + RG i; slot SLOTS: beta row 192 + rg).  The y
+// rows (slots 0 and 1) never feed the recurrence, so their work runs one step
+// behind, off the step's chain: at step t the thread forms a^y of step t-1,
+// writes y_t, applies the y rows' update of step t-1 and forms their b for
+// y_{t+1}.  The chain itself is: z_t -> softmaxes -> u -> a of the k, q and
+// beta rows -> z_{t+1} -> barrier.
 template <int NW, int NS, int NLR, bool EMIT = false>
 __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int lane, int warp, int rg, int cg,
                                          float2 (&w)[d64::Cfg<NW>::SLOTS + 1][d64::NP],
-                                         float (&coef)[d64::Cfg<NW>::SLOTS + 1], float2 (&pkc)[d64::NP],
-                                         const float* xn, float* em = nullptr)
+                                         float (&coef)[d64::Cfg<NW>::SLOTS + 1], D64Carry<NW>& cy,
+                                         const float* xn, float* em = nullptr, float* em_prev = nullptr)
 {
     using namespace d64;
     using C = Cfg<NW>;
     constexpr int SLOTS = C::SLOTS, RG = C::RG;
     constexpr int M = 3 * D + NLR;
+    static_assert(C::block_of_slot(0) == 0 && C::block_of_slot(1) == 0 && C::block_of_slot(2) != 0,
+                  "slots 0 and 1 are the y rows");
     const float* zt = sm.z[t & 1];
     float* zn = sm.z[(t + 1) & 1];
 
-    // ---- 1. softmax / gates || pending update + b-dots
+    // ---- 1. the softmaxes and gates (the chain), and beside them the work
+    // that does not depend on them
     const float k0 = zt[D + lane], k1 = zt[D + 32 + lane];
     const float q0 = zt[2 * D + lane], q1 = zt[2 * D + 32 + lane];
     const float4 beta = *reinterpret_cast<const float4*>(&zt[3 * D]);
-
-    // the softmaxes first in source order: their long-latency reductions are
-    // then issued ahead of the update's FMAs, which fill the waits (measured
-    // 1.7 % faster on the long workload than the reverse order)
     float pk0, pk1, pq0, pq1;
     softmax64(k0, k1, pk0, pk1);
     softmax64(q0, q1, pq0, pq1);
-
-    float2 x2[NP];
-    load_pairs(xn, cg, x2);
-    float2 accb[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) accb[i] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < NP; ++q) {
-#pragma unroll
-        for (int i = 0; i < NS; ++i) {
-            w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
-            accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
-        }
-    }
     float g[4];
     if constexpr (NLR == 4) {
         g[0] = sigmoid_fast(beta.x);
@@ -143,67 +145,122 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
         g[0] = g[1] = g[2] = g[3] = sigmoid_fast(beta.x);
     }
 
-    // ---- 2. phi into the thread's column layout; a-dots; partial phi_k . x~
+    // the y rows, one step behind: a^y of step t-1 on W^y_{t-2} (which has not
+    // yet taken step t-1's update), its gate product, and y_t.  At t = 0 the
+    // carried u and gate are zero, so coef stays 0, and y_0 came from the
+    // prologue: only the stores are predicated, the rest runs branch-free.
+    {
+        float ay[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) acc = __ffma2_rn(w[i][q], cy.u2[q], acc);
+            ay[i] = acc.x + acc.y;
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) ay[i] += __shfl_xor_sync(0xffffffffu, ay[i], o);
+        }
+        float* yrow = sm.ystage[(t / TAU) % 3][t % TAU];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            coef[i] = cy.gy * ay[i];
+            if (i == cg && t > 0) yrow[rg + RG * i] = fmaf(coef[i], cy.ys, cy.yb[i]);
+            if constexpr (EMIT) {
+                if (i == cg && t > 0) em_prev[2 * D + 4 + rg + RG * i] = ay[i];
+            }
+        }
+    }
+
+    // the pending update of step t-1 (all slots) and b = W_{t-1} x~_{t+1}
+    float2 x2[NP];
+    load_pairs(xn, cg, x2);
+    float b[NS];
+    {
+        float2 accb[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) accb[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 2; i < NS; ++i) {
+                w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), cy.pkc[q], w[i][q]);
+                accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), cy.pkc[q], w[i][q]);
+                accb[i] = __ffma2_rn(w[i][q], x2[q], accb[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NS; ++i) b[i] = accb[i].x + accb[i].y;
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < NS; ++i) b[i] += __shfl_xor_sync(0xffffffffu, b[i], o);
+        }
+    }
+
+    // ---- 2. phi_k and u into the thread's column layout.  u takes an explicit
+    // rounded subtraction, so equal k and q rows give u = 0 exactly.
     float* pkq = &sm.pkq[warp][0][0];
+    const float u0 = __fsub_rn(pq0, pk0), u1 = __fsub_rn(pq1, pk1);
     pkq[lane] = pk0;
     pkq[lane + 32] = pk1;
-    pkq[D + lane] = pq0;
-    pkq[D + lane + 32] = pq1;
+    pkq[D + lane] = u0;
+    pkq[D + lane + 32] = u1;
     if constexpr (EMIT) {
-        // backward record: phi(k), u, gates (u as the column pass forms it: pq - pk)
+        // backward record of step t: phi(k), u, gates (the rows' a follow)
         if (warp == 0) {
             em[lane] = pk0;
             em[lane + 32] = pk1;
-            em[D + lane] = __fsub_rn(pq0, pk0);   // as the column pass forms it (no contraction)
-            em[D + lane + 32] = __fsub_rn(pq1, pk1);
+            em[D + lane] = u0;
+            em[D + lane + 32] = u1;
             if (lane < 4) em[2 * D + lane] = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3];
         }
     }
     __syncwarp();
-    float2 u2[NP];
-    {
-        float2 q2[NP];
-        load_pairs(pkq, cg, pkc);
-        load_pairs(pkq + D, cg, q2);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) u2[q] = make_float2(q2[q].x - pkc[q].x, q2[q].y - pkc[q].y);
-    }
-    float2 acca[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) acca[i] = make_float2(0.f, 0.f);
-    float2 accs = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < NP; ++q) {
-#pragma unroll
-        for (int i = 0; i < NS; ++i) acca[i] = __ffma2_rn(w[i][q], u2[q], acca[i]);
-        accs = __ffma2_rn(pkc[q], x2[q], accs);
-    }
-    float a[NS], bb[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-        a[i] = acca[i].x + acca[i].y;
-        bb[i] = accb[i].x + accb[i].y;
-    }
-    float s = accs.x + accs.y;
+    load_pairs(pkq, cg, cy.pkc);
+    load_pairs(pkq + D, cg, cy.u2);
 
-    // ---- 3. finish the dots over the 4 column groups; store z_{t+1}
+    // ---- 3. a of the k, q and beta rows (the chain) and s = phi_k . x~_{t+1}
+    float a[NS];
+    float s;
+    {
+        float2 acca[NS];
+#pragma unroll
+        for (int i = 2; i < NS; ++i) acca[i] = make_float2(0.f, 0.f);
+        float2 accs = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+#pragma unroll
+            for (int i = 2; i < NS; ++i) acca[i] = __ffma2_rn(w[i][q], cy.u2[q], acca[i]);
+            accs = __ffma2_rn(cy.pkc[q], x2[q], accs);
+        }
+#pragma unroll
+        for (int i = 2; i < NS; ++i) a[i] = acca[i].x + acca[i].y;
+        s = accs.x + accs.y;
+    }
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
 #pragma unroll
-        for (int i = 0; i < NS; ++i) {
-            a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
-            bb[i] += __shfl_xor_sync(0xffffffffu, bb[i], o);
-        }
+        for (int i = 2; i < NS; ++i) a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
         s += __shfl_xor_sync(0xffffffffu, s, o);
     }
 
-    const bool write_y = (t + 1 < T);
-    float* yrow = sm.ystage[((t + 1) / TAU) % 3][(t + 1) % TAU];
+    // ---- 4. z_{t+1} of the k, q and beta rows; the y rows' values for the
+    // next step
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 2; i < NS; ++i) {
         const int blk = (NLR == 1) ? 0 : (i < SLOTS ? C::block_of_slot(i) : 3);
         coef[i] = g[blk] * a[i];
-        const float zr = fmaf(coef[i], s, bb[i]);
+        const float zr = fmaf(coef[i], s, b[i]);
         if constexpr (EMIT) {
             if ((i & 3) == cg) {
                 if (i < SLOTS) em[2 * D + 4 + rg + RG * i] = a[i];
@@ -211,16 +268,18 @@ __device__ __forceinline__ void d64_step(d64::Smem<NW>& sm, int t, int T, int la
             }
         }
         if ((i & 3) == cg) {
-            if (i < SLOTS && C::block_of_slot(i) == 0) {
-                if (write_y) yrow[rg + RG * i] = zr;
-            } else if (i < SLOTS) {
-                zn[rg + RG * i] = zr;
-            } else if (3 * D + rg < M) {
-                zn[3 * D + rg] = zr;
-            }
+            if (i < SLOTS) zn[rg + RG * i] = zr;
+            else if (3 * D + rg < M) zn[3 * D + rg] = zr;
         }
     }
-    if (write_y && ((t + 2) % TAU == 0 || t + 2 == T)) fence_proxy_async_smem();
+    cy.yb[0] = b[0];
+    cy.yb[1] = b[1];
+    cy.ys = s;
+    cy.gy = g[0];
+    // y_t was the last row of its chunk: order the chunk's writes before the
+    // TMA store that reads it (issued after the next barrier).  At the end of
+    // the step, where it holds up no other work.
+    if (t > 0 && ((t + 1) % TAU == 0 || t + 1 == T)) fence_proxy_async_smem();
 }
 
 template <int NW, int NLR, bool SMX, bool EMIT = false>
@@ -245,6 +304,7 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     if (tid == 0) {
         mbar_init(&sm.xbar[0], 1);
         mbar_init(&sm.xbar[1], 1);
+        mbar_init(&sm.xbar[2], 1);
         fence_mbar_init();
         if (kp.T > 0) {
             prefetch_tensormap(&tmx);
@@ -253,8 +313,8 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
     }
     __syncthreads();
 
-    // completed phases of the two x buffers over all items of this CTA
-    uint32_t used0 = 0, used1 = 0;
+    // bit i: parity of the phases x buffer i completed over earlier items
+    uint32_t used = 0;
     int abort = 0;
     int issued = -1, landed = -1;   // chunks of the current item (warp XW)
 
@@ -296,19 +356,20 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
         }
 
         // ---- x staging (warp XW) and its TMA bookkeeping; chunk c of this
-        // item is steps t0 + c*TAU .. and lands in buffer c & 1
-        auto parity = [&](int c) -> uint32_t { return ((c & 1) ? used1 : used0) + (c >> 1); };
+        // item is steps t0 + c*TAU .. and lands in buffer c % 3, as that
+        // buffer's (c / 3)-th load of the item
+        auto parity = [&](int c) -> uint32_t { return ((used >> (c % 3)) + static_cast<uint32_t>(c / 3)) & 1u; };
         auto issue_chunk = [&](int c) {
             if (lane == 0 && c != kp.skip_chunk) {
-                mbar_arrive_expect_tx(&sm.xbar[c & 1], kChunkBytes);
-                tma_load_4d(&sm.xring[c & 1][0][0], &tmx, &sm.xbar[c & 1], 0, h, t0 + c * TAU, b);
+                mbar_arrive_expect_tx(&sm.xbar[c % 3], kChunkBytes);
+                tma_load_4d(&sm.xring[c % 3][0][0], &tmx, &sm.xbar[c % 3], 0, h, t0 + c * TAU, b);
             }
             issued = c;
         };
         auto stage_x = [&](int tn, float* dst) {
             float v0 = 0.f, v1 = 0.f;
             if (tn < T) {
-                const float* src = sm.xring[(tn / TAU) & 1][tn % TAU];
+                const float* src = sm.xring[(tn / TAU) % 3][tn % TAU];
                 v0 = src[lane];
                 v1 = src[lane + 32];
                 if constexpr (SMX) softmax64(v0, v1, v0, v1);
@@ -321,7 +382,7 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
         if (warp == XW && T > 0) {
             issue_chunk(0);
             if (nchunks > 1) issue_chunk(1);
-            if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], parity(0) & 1, kp.wait_limit_ns))) {
+            if (__all_sync(0xffffffffu, mbar_wait_bounded(&sm.xbar[0], parity(0), kp.wait_limit_ns))) {
                 landed = 0;
                 if constexpr (SMX) {
                     stage_x(0, sm.xs[0]);
@@ -368,64 +429,71 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
         __syncthreads();
 
         // the pending rank-one update (applied at the start of the next step)
+        // and the y rows' values carried one step
         float coef[S1];
 #pragma unroll
         for (int i = 0; i < S1; ++i) coef[i] = 0.f;
-        float2 pkc[NP];
+        D64Carry<NW> cy;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) pkc[q] = make_float2(0.f, 0.f);
+        for (int q = 0; q < NP; ++q) cy.pkc[q] = cy.u2[q] = make_float2(0.f, 0.f);
+        cy.yb[0] = cy.yb[1] = cy.ys = cy.gy = 0.f;
 
         // Warp 0 also carries the beta rows; a compile-time slot count keeps
         // each role's step free of branches.
         auto step = [&](int t, const float* xn) {
             float* em = nullptr;
             if constexpr (EMIT) em = kp.emit + (static_cast<size_t>(p) * kp.T + t0 + t) * kp.emit_stride;
-            if (has_beta) d64_step<NW, S1, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn, em);
-            else d64_step<NW, SLOTS, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, pkc, xn, em);
+            float* em_prev = EMIT ? em - kp.emit_stride : nullptr;
+            if (has_beta) d64_step<NW, S1, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, cy, xn, em, em_prev);
+            else d64_step<NW, SLOTS, NLR, EMIT>(sm, t, T, lane, warp, rg, cg, w, coef, cy, xn, em, em_prev);
         };
         if constexpr (!SMX) {
             // x~ = x is read straight from the ring, chunk by chunk: the inner
             // loop holds only the step and its barrier; the chunk boundary
             // (bounded wait for the next chunk, agreed on by the CTA, the next
             // TMA load, the y store) runs between chunks.
-            for (int c0 = 0; c0 < T && !abort; c0 += TAU) {
-                const int tend = min(c0 + TAU, T);
-                const float* ring = sm.xring[(c0 / TAU) & 1][0];
-                for (int t = c0; t < tend - 1; ++t) {
-                    step(t, ring + (t + 1 - c0) * D);
-                    __syncthreads();
-                }
-                const float* xn = ring;   // unused past the end of the item
-                if (tend < T) {
-                    // chunk c is read from the next step on; its buffer's previous
-                    // chunk c-2 was last read two chunks ago, and chunk c+1 goes into
-                    // the current buffer, whose last read was the step before this one
-                    const int c = tend / TAU;
-                    const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c) & 1, kp.wait_limit_ns);
+            for (int c = 0; c < nchunks && !abort; ++c) {
+                // The last step of chunk c reads the first row of chunk c + 1,
+                // issued a chunk ago; chunk c + 2 goes into the buffer of chunk
+                // c - 1, whose last row was read before here.
+                if (c + 1 < nchunks) {
+                    const bool ok = mbar_wait_bounded(&sm.xbar[(c + 1) % 3], parity(c + 1), kp.wait_limit_ns);
                     if (__syncthreads_or(!ok)) {
                         abort = 1;
                         break;
                     }
                     if (warp == XW) {
-                        landed = c;
-                        if (c + 1 < nchunks) issue_chunk(c + 1);
+                        landed = c + 1;
+                        if (c + 2 < nchunks) issue_chunk(c + 2);
                     }
-                    xn = sm.xring[c & 1][0];
                 }
-                step(tend - 1, xn);
-                __syncthreads();
-                // y of the chunk's steps complete -> TMA store
-                if (warp == 0 && lane == 0 && tend % TAU == 0) {
-                    tma_store_4d(&tmy, &sm.ystage[(c0 / TAU) % 3][0][0], 0, h, t0 + c0, b);
+                // y of chunk c - 1 is complete (its last row was written, and
+                // fenced, in the chunk's last step) -> TMA store; the store
+                // before it has finished reading the buffer this chunk writes
+                if (c > 0 && warp == 0 && lane == 0) {
+                    tma_store_4d(&tmy, &sm.ystage[(c - 1) % 3][0][0], 0, h, t0 + (c - 1) * TAU, b);
                     bulk_commit();
                     bulk_wait_read<1>();
                 }
+                const int tend = min(T, (c + 1) * TAU);
+                // the chunk's last step (the one that reads the next chunk)
+                // stands apart from the loop over the others: measured 5.2 ->
+                // 4.2 ms on long against one loop over all steps (same results
+                // bit for bit; only the compiled schedule differs)
+                const float* ring = sm.xring[c % 3][0];
+                for (int t = c * TAU; t < tend - 1; ++t) {
+                    step(t, ring + (t + 1 - c * TAU) * D);
+                    __syncthreads();
+                }
+                step(tend - 1, sm.xring[(c + 1) % 3][0]);
+                __syncthreads();
             }
         } else {
             for (int t = 0; t < T && !abort; ++t) {
-                // y chunk holding y_t complete -> TMA store
-                if (warp == 0 && lane == 0 && (t + 1) % TAU == 0) {
-                    const int c = t / TAU;
+                // y_{t-1} (written during step t - 1, the y rows running one
+                // step behind) completed its chunk -> TMA store
+                if (warp == 0 && lane == 0 && t > 0 && t % TAU == 0) {
+                    const int c = (t - 1) / TAU;
                     tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
                     bulk_commit();
                     bulk_wait_read<1>();
@@ -438,7 +506,7 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
                     const int tn = t + 2;
                     if (tn < T && tn % TAU == 0) {
                         const int c = tn / TAU;
-                        const bool ok = mbar_wait_bounded(&sm.xbar[c & 1], parity(c) & 1, kp.wait_limit_ns);
+                        const bool ok = mbar_wait_bounded(&sm.xbar[c % 3], parity(c), kp.wait_limit_ns);
                         if (__all_sync(0xffffffffu, ok)) {
                             landed = c;
                             if (c + 1 < nchunks) issue_chunk(c + 1);
@@ -452,9 +520,10 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
             }
         }
 
-        // ---- drain this item's y stores
+        // ---- drain this item's y stores (the last chunk's store trails its
+        // steps, as every chunk's does)
         if (warp == 0 && lane == 0) {
-            if (!abort && T > 0 && T % TAU != 0) {
+            if (!abort && T > 0) {
                 const int c = (T - 1) / TAU;
                 tma_store_4d(&tmy, &sm.ystage[c % 3][0][0], 0, h, t0 + c * TAU, b);
                 bulk_commit();
@@ -462,17 +531,42 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
             bulk_wait_all<0>();
         }
         if (abort) break;
-        used0 += (nchunks + 1) / 2;
-        used1 += nchunks / 2;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) used ^= (static_cast<uint32_t>(nchunks > i ? (nchunks - 1 - i) / 3 + 1 : 0) & 1u) << i;
 
-        // ---- the last pending update, then the state -> W_out[b, h]
+        // ---- the y rows' a of the last step (they run one step behind), the
+        // last pending update, then the state -> W_out[b, h]
+        if (T > 0) {
+            float ay[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) acc = __ffma2_rn(w[i][q], cy.u2[q], acc);
+                ay[i] = acc.x + acc.y;
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) ay[i] += __shfl_xor_sync(0xffffffffu, ay[i], o);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                coef[i] = cy.gy * ay[i];
+                if constexpr (EMIT) {
+                    if (i == cg)
+                        kp.emit[(static_cast<size_t>(p) * kp.T + t0 + T - 1) * kp.emit_stride + 2 * D + 4 + rg +
+                                RG * i] = ay[i];
+                }
+            }
+        }
         float* Wd = kp.W_out + static_cast<size_t>(p) * M * D;
 #pragma unroll
         for (int i = 0; i < S1; ++i) {
             const int r = (i < SLOTS) ? rg + RG * i : 3 * D + rg;
             if (i == SLOTS && !(has_beta && r < M)) continue;
 #pragma unroll
-            for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), pkc[q], w[i][q]);
+            for (int q = 0; q < NP; ++q) w[i][q] = __ffma2_rn(make_float2(coef[i], coef[i]), cy.pkc[q], w[i][q]);
 #pragma unroll
             for (int j = 0; j < NP / 2; ++j) {
                 *reinterpret_cast<float4*>(Wd + static_cast<size_t>(r) * D + 4 * (cg + 4 * j)) =
@@ -491,7 +585,8 @@ __global__ void __launch_bounds__(d64::Cfg<NW>::NT, 8 / NW)
             // every load still in flight lands before the CTA gives up its shared memory
             for (int c = landed + 1; c <= issued; ++c) {
                 if (c == kp.skip_chunk) continue;
-                mbar_wait_bounded(&sm.xbar[c & 1], (((c & 1) ? used1 : used0) + (c >> 1)) & 1, kp.wait_limit_ns);
+                mbar_wait_bounded(&sm.xbar[c % 3], ((used >> (c % 3)) + static_cast<uint32_t>(c / 3)) & 1u,
+                                  kp.wait_limit_ns);
             }
         }
         if (tid == 0) atomicOr(kp.status, kStatusTimeout);

@@ -390,11 +390,16 @@ __global__ void __launch_bounds__(d64r::NT, 4)
                     bulk_wait_read<1>();
                 }
             }
+            // the chunk's last step stands apart from the loop over the others:
+            // measured 1.07 -> 1.03 ms on mid against one loop over all steps
+            // (same results bit for bit; only the compiled schedule differs)
             const int t_end = min(T, (c + 1) * TAU);
-            for (int t = c * TAU; t < t_end; ++t) {
+            for (int t = c * TAU; t < t_end - 1; ++t) {
                 d64r_step<NLR, EMIT>(sm, kp, p, t, T, tid, lane, warp, w, wb, coef, coefb);
                 __syncthreads();
             }
+            d64r_step<NLR, EMIT>(sm, kp, p, t_end - 1, T, tid, lane, warp, w, wb, coef, coefb);
+            __syncthreads();
         }
 
         // ---- the last chunk's y, then drain this piece's stores
