@@ -21,21 +21,25 @@
 // One step, one CTA barrier:
 //   1. every warp computes phi_k, phi_q and the gates from z_t in shared
 //      memory (redux max, exp, fixed-point redux sum, approximate reciprocal);
-//      meanwhile it applies the previous step's rank-one update fused with the
-//      dot products b_r against x~_{t+1};
-//   2. phi_k / phi_q go through a warp-private shared buffer into the thread's
-//      column layout; a_r and the partial phi_k . x~_{t+1};
-//   3. two xor-shuffle levels finish the dots; owner lanes store z_{t+1}
-//      (y rows to the TMA staging buffer, k/q/beta rows to shared memory);
+//      beside them, the work that does not depend on them: the y rows' a of
+//      step t-1, their gate product and y_t (the y rows never feed the
+//      recurrence, so they run one step behind), the previous step's rank-one
+//      update of every row, b_r = W_{t-1}[r,:] . x~_{t+1} and its sum over the
+//      four column groups;
+//   2. phi_k and u = phi_q - phi_k go through a warp-private shared buffer
+//      into the thread's column layout;
+//   3. a_r of the k, q and beta rows and the partial phi_k . x~_{t+1}; two
+//      xor-shuffle levels finish them; owner lanes store z_{t+1} of those rows;
 //   4. barrier.
-// The update of step t is applied at the start of step t+1 (or after the
-// loop), so it overlaps the softmax latency instead of preceding the barrier.
+// So the step's chain is z_t -> softmaxes -> u -> a of the k, q and beta rows
+// -> z_{t+1} -> barrier.
 // z is double-buffered by step parity (a fast warp writes z_{t+1} while a slow
 // one still reads z_t); y staging is triple-buffered (one chunk being written,
 // up to two still read by bulk stores).
-// Without the input softmax x~ = x is read straight from the TMA ring, and the
-// steps run chunk by chunk, with the chunk-boundary work between chunks
-// rather than in every step (measured: 6.44 -> 5.34 ms on the long workload).
+// Without the input softmax x~ = x is read straight from a three-chunk TMA
+// ring, and the steps run chunk by chunk: the chunk boundary (wait for the
+// next chunk, issue the one after, store the previous chunk's y) sits at the
+// start of each chunk, outside the step loop.
 #pragma once
 
 #include <cuda.h>
