@@ -727,26 +727,37 @@ def bench_layer(args, wl):
     steps = max(3, min(args.steps, 20))
     t_layer = timed(layer, steps)
     t_srwm = timed(srwm, steps)
-    binding.srwm_debug_set_layer_gemm(True)
-    try:
-        t_plain = timed(layer, steps)
-    finally:
-        binding.srwm_debug_set_layer_gemm(False)
+    t_cmp = {}
+    for mode, name in ((2, "cublaslt_emulated_fp32"), (1, "cublaslt_plain_fp32")):
+        binding.srwm_debug_set_layer_gemm(mode)
+        try:
+            t_cmp[name] = timed(layer, steps)
+        finally:
+            binding.srwm_debug_set_layer_gemm(0)
     tokens = wl.B * wl.T
     ff_flops = 2 * 2 * tokens * D * d_ff
+    ff_ms = t_layer - t_srwm
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    sustained = peaks.get("bf16_tflops_sustained")
+    # the tensor cores run three bf16 products per fp32 product (hi*hi, hi*lo, lo*hi)
+    tc_tflops = 3 * ff_flops / (ff_ms / 1e3) / 1e12
     print(json.dumps({
         "metric": "Recursive Self-Transformer layer forward, tokens/s (1 GB300)",
         "value": tokens / (t_layer / 1e3), "unit": "tokens/s", "ms_per_step": t_layer, "steps": steps,
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d": wl.d, "D": D, "d_ff": d_ff,
                    "n_lr": wl.n_lr, "softmax_input": wl.softmax_input, "l2": "flushed between timed steps"},
         "dtype": "f32", "data": "synthetic",
-        "parts_ms": {"srwm_forward_alone": t_srwm, "layer_minus_srwm": t_layer - t_srwm},
+        "parts_ms": {"srwm_forward_alone": t_srwm, "layer_minus_srwm": ff_ms},
         "ff_gemm_flops": ff_flops,
-        "ff_plus_ln_tflops_emulated_fp32": ff_flops / ((t_layer - t_srwm) / 1e3) / 1e12,
-        "ms_per_step_plain_fp32_gemm": t_plain,
-        "ff_plus_ln_tflops_plain_fp32": ff_flops / ((t_plain - t_srwm) / 1e3) / 1e12,
+        "ff_plus_ln_tflops_fp32_equivalent": ff_flops / (ff_ms / 1e3) / 1e12,
+        "ff_plus_ln_bf16_tensor_tflops": tc_tflops,
+        "ff_plus_ln_frac_of_bf16_sustained": (tc_tflops / sustained) if sustained else None,
+        "comparison_ms_per_step": t_cmp,
     }), flush=True)
-
 
 if __name__ == "__main__":
     main()

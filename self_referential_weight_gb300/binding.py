@@ -357,8 +357,11 @@ def srwm_layer_forward(u, H, n_lr, softmax_input, ln1_gamma, ln1_beta, W0, ln2_g
     return out, W_final
 
 
-def srwm_debug_set_layer_gemm(plain_fp32: bool) -> None:
-    _check(_lib().srwm_debug_set_layer_gemm(int(bool(plain_fp32))), "srwm_debug_set_layer_gemm")
+def srwm_debug_set_layer_gemm(mode: int) -> None:
+    """The layer's feed-forward products: 0 this library's tensor-core kernel
+    (default), 1 cuBLASLt plain FP32, 2 cuBLASLt FP32 emulated on BF16 (the
+    last two for comparison)."""
+    _check(_lib().srwm_debug_set_layer_gemm(int(mode)), "srwm_debug_set_layer_gemm")
 
 
 def srwm_last_device_status(stream=None) -> int:

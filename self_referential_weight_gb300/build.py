@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsrwm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 UNITS = ["srwm_api.cu", "srwm_d16.cu", "srwm_d32.cu", "srwm_d64.cu", "srwm_probe.cu", "srwm_noalloc.cu", "srwm_bwd.cu",
-         "srwm_layer.cu"]
+         "srwm_layer.cu", "srwm_ffgemm.cu"]
 
 
 def _nvcc() -> str:

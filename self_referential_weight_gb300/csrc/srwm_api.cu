@@ -456,6 +456,15 @@ int effective_chunk(int T, int d, int chunk_steps)
 
 }  // namespace
 
+namespace srwm {
+
+// For the layer's tensor-core products (srwm_ffgemm.cu): the device status
+// word and the bounded-wait limit the kernels of this library share.
+int device_status_ptr(unsigned** out) { return status_ptr(out); }
+unsigned long long device_wait_limit_ns() { return static_cast<unsigned long long>(g_wait_limit_ns.load()); }
+
+}  // namespace srwm
+
 extern "C" {
 
 int srwm_forward(const float* x, const float* W0, int B, int T, int H, int d, int n_lr,

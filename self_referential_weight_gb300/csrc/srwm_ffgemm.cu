@@ -1,0 +1,422 @@
+// srwm_ffgemm.cu -- the feed-forward products of the Recursive Self-Transformer
+// layer on the 5th-generation tensor cores: TMA tile loads, tcgen05.mma with
+// the accumulator in tensor memory, tcgen05.ld for the epilogue.
+//
+// fp32-level accuracy from BF16 tensor cores by a three-term split: every
+// fp32 operand x is held as hi = bf16(x) and lo = bf16(x - hi), and
+//   X W^T  ~  X_hi W_hi^T + X_hi W_lo^T + X_lo W_hi^T
+// accumulated in fp32 (the dropped X_lo W_lo^T term and lo's own rounding are
+// ~2^-16 of each product: ~1e-5 relative on the layer's output).
+//
+// Out[N, Mo] = epilogue(A[N, K] B[Mo, K]^T): A and B row-major, K contiguous
+// ("K-major" for both tensor-core operands), as X and a PyTorch Linear weight.
+// Epilogues: (1) f = ReLU(acc + bias) written as a bf16 (hi, lo) pair, the
+// next product's A operand; (2) out = out + acc + bias in fp32 (out holds the
+// residual).
+//
+// Persistent, warp-specialised CTA (one per SM): warp 0 issues the TMA loads,
+// warp 1 the MMAs (one thread each), warps 2-5 run the epilogue, each on the
+// 32 tensor-memory lanes (= tile rows) its warp may access.  Tiles of 128 x 256
+// outputs; K in steps of 64 (one 128-byte swizzle row of bf16); two shared-
+// memory stages (A_hi, A_lo, B_hi, B_lo: 96 KB each) and two accumulators in
+// tensor memory (2 x 256 columns), so one tile's epilogue overlaps the next
+// tile's products.  Every wait is bounded; a timeout sets the status word,
+// stops new work, waits (bounded) for work in flight and frees the tensor
+// memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "srwm.h"
+#include "srwm_common.h"
+#include "srwm_ffgemm.h"
+#include "srwm_ptx.cuh"
+
+namespace srwm {
+namespace ff {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 2, NACC = 2;
+constexpr int TILE_A = BM * BK * 2;                    // bytes of one bf16 A tile (16 KB)
+constexpr int TILE_B = BN * BK * 2;                    // 32 KB
+constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;   // A_hi | A_lo | B_hi | B_lo
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = NACC * BN;              // 512: the whole tensor memory of the SM
+
+struct __align__(1024) Smem {
+    uint8_t stage[STAGES][STAGE_BYTES];
+    uint64_t full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(STAGE_BYTES % 1024 == 0 && TILE_A % 1024 == 0 && TILE_B % 1024 == 0,
+              "128-byte swizzled tiles start on 1024-byte boundaries");
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// the 128-byte swizzle: rows of 128 bytes (64 bf16 along K), atoms of 8 rows
+// (1024 bytes, the stride between 8-row groups); the leading-dimension offset
+// is not used by this layout.  Bits: start address >> 4 [0, 14), leading byte
+// offset >> 4 [16, 30), stride byte offset >> 4 [32, 46), descriptor version 1
+// [46, 48), swizzle mode [61, 64) (2: 128-byte).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
+// [4, 6) = 1), bf16 A and B ([7, 10) = 1, [10, 13) = 1), both K-major (bits 15,
+// 16 = 0), N >> 3 in [17, 23), M >> 4 in [24, 29).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued before it has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 columns of the warp's 32 tensor-memory lanes (one row per thread), then
+// the wait for the load, in one statement so no use can move ahead of it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// x -> (hi, lo) with hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split_bf16(float x, float& hi, float& lo)
+{
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    ffgemm_kernel(const __grid_constant__ CUtensorMap ta_hi, const __grid_constant__ CUtensorMap ta_lo,
+                  const __grid_constant__ CUtensorMap tb_hi, const __grid_constant__ CUtensorMap tb_lo,
+                  const GemmArgs ga)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    if ((smem_u32(smem_raw) & 1023u) != 0) {   // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(ga.status, kStatusSmemBase);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (ga.N + BM - 1) / BM, n_tiles = (ga.Mo + BN - 1) / BN;
+    const int ntiles = m_tiles * n_tiles;
+    const int kblocks = (ga.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_empty[a], 4);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&ta_hi);
+        prefetch_tensormap(&ta_lo);
+        prefetch_tensormap(&tb_hi);
+        prefetch_tensormap(&tb_lo);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sm.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    volatile int* abort = &sm.abort;
+    auto fail = [&]() {
+        *abort = 1;
+        atomicOr(ga.status, kStatusTimeout);
+    };
+
+    if (warp == 0) {
+        // ---- TMA producer (one thread; the warp's other lanes wait at the end)
+        if (lane == 0) {
+        int it = 0, last_stage = -1;
+        uint32_t last_parity = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*abort; tile += gridDim.x) {
+            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (!mbar_wait_bounded(&sm.empty[s], ph ^ 1u, ga.wait_limit_ns)) {
+                    fail();
+                    break;
+                }
+                if (*abort) break;
+                uint8_t* st = sm.stage[s];
+                mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
+                tma_load_2d(st, &ta_hi, &sm.full[s], kb * BK, m0);
+                tma_load_2d(st + TILE_A, &ta_lo, &sm.full[s], kb * BK, m0);
+                tma_load_2d(st + 2 * TILE_A, &tb_hi, &sm.full[s], kb * BK, n0);
+                tma_load_2d(st + 2 * TILE_A + TILE_B, &tb_lo, &sm.full[s], kb * BK, n0);
+                last_stage = s;
+                last_parity = ph;
+            }
+        }
+        // the shared memory may only be given up once the last loads landed
+        if (last_stage >= 0) mbar_wait_bounded(&sm.full[last_stage], last_parity, ga.wait_limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer (one thread; the warp's other lanes wait at the end)
+        if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(BM, BN);
+        int it = 0, li = 0;
+        uint64_t* last_commit = nullptr;
+        uint32_t last_commit_parity = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*abort; tile += gridDim.x, ++li) {
+            const int ab = li & 1;
+            const uint32_t aph = (li >> 1) & 1;
+            if (!mbar_wait_bounded(&sm.acc_empty[ab], aph ^ 1u, ga.wait_limit_ns)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (!mbar_wait_bounded(&sm.full[s], ph, ga.wait_limit_ns) || *abort) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = smem_u32(sm.stage[s]);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint32_t ko = static_cast<uint32_t>(k * 32);   // 16 bf16 along K
+                    const uint64_t a_hi = sw128_desc(base + ko), a_lo = sw128_desc(base + TILE_A + ko);
+                    const uint64_t b_hi = sw128_desc(base + 2 * TILE_A + ko);
+                    const uint64_t b_lo = sw128_desc(base + 2 * TILE_A + TILE_B + ko);
+                    umma(d, a_hi, b_hi, idesc, (kb | k) != 0 ? 1u : 0u);
+                    umma(d, a_hi, b_lo, idesc, 1u);
+                    umma(d, a_lo, b_hi, idesc, 1u);
+                }
+                umma_commit(&sm.empty[s]);   // the stage is free once these products have read it
+                last_commit = &sm.empty[s];
+                last_commit_parity = ph;
+            }
+            if (!ok) {
+                fail();
+                break;
+            }
+            umma_commit(&sm.acc_full[ab]);
+            last_commit = &sm.acc_full[ab];
+            last_commit_parity = aph;
+        }
+        // tensor memory may only be freed once the products issued completed
+        if (last_commit) mbar_wait_bounded(last_commit, last_commit_parity, ga.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        const int q = warp & 3;
+        int li = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*abort; tile += gridDim.x, ++li) {
+            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+            const int ab = li & 1;
+            const uint32_t aph = (li >> 1) & 1;
+            if (!mbar_wait_bounded(&sm.acc_full[ab], aph, ga.wait_limit_ns)) {
+                if (lane == 0) fail();
+                break;
+            }
+            tc_fence_after();
+            const long long row = m0 + 32 * q + lane;
+            const bool row_ok = row < ga.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = n0 + 32 * c;
+                uint32_t r[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 32 * c), r);
+                if (col0 >= ga.Mo) continue;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {   // 8 columns at a time
+                    const int cc = col0 + 8 * g;
+                    if (!row_ok || cc >= ga.Mo) continue;
+                    float v[8];
+                    const float4 b0 = __ldg(reinterpret_cast<const float4*>(ga.bias + cc));
+                    const float4 b1 = __ldg(reinterpret_cast<const float4*>(ga.bias + cc + 4));
+                    const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[8 * g + j]) + bb[j];
+                    if constexpr (EPI == 1) {
+                        float hi[8], lo[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) split_bf16(fmaxf(v[j], 0.f), hi[j], lo[j]);
+                        const size_t o = static_cast<size_t>(row) * ga.Mo + cc;
+                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ga.out_hi) + o) =
+                            make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]),
+                                       pack_bf16(hi[6], hi[7]));
+                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ga.out_lo) + o) =
+                            make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
+                                       pack_bf16(lo[6], lo[7]));
+                    } else {
+                        float4* o = reinterpret_cast<float4*>(ga.out + static_cast<size_t>(row) * ga.Mo + cc);
+                        const float4 h0 = o[0], h1 = o[1];
+                        o[0] = make_float4(h0.x + v[0], h0.y + v[1], h0.z + v[2], h0.w + v[3]);
+                        o[1] = make_float4(h1.x + v[4], h1.y + v[5], h1.z + v[6], h1.w + v[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);   // the accumulator may take the next tile
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+// fp32 -> (bf16 hi, bf16 lo), elementwise
+__global__ void split_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ hi,
+                             __nv_bfloat16* __restrict__ lo, long long n)
+{
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float x = src[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        hi[i] = h;
+        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D map over a row-major bf16 [rows, K] matrix: boxes of `box_rows` rows x
+// 64 columns, 128-byte swizzle, zero fill outside the matrix.
+int make_map(CUtensorMap* map, const void* base, long long rows, int K, int box_rows)
+{
+    auto enc = encoder();
+    if (!enc) return SRWM_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+}  // namespace ff
+
+int ff_split(const float* src, void* hi, void* lo, long long n, cudaStream_t st)
+{
+    if (n <= 0) return SRWM_OK;
+    const long long blocks = (n + 255) / 256;
+    ff::split_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(
+        src, static_cast<__nv_bfloat16*>(hi), static_cast<__nv_bfloat16*>(lo), n);
+    return cudaGetLastError() == cudaSuccess ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+int ff_gemm(int epi, const void* a_hi, const void* a_lo, const void* b_hi, const void* b_lo, const GemmArgs& args,
+            cudaStream_t st)
+{
+    using namespace ff;
+    if (args.N <= 0 || args.Mo <= 0) return SRWM_OK;
+    if (args.K <= 0 || args.K % 8 != 0 || args.Mo % 8 != 0) return SRWM_ERR_UNSUPPORTED;
+    CUtensorMap m[4];
+    int rc;
+    if ((rc = make_map(&m[0], a_hi, args.N, args.K, BM)) != SRWM_OK ||
+        (rc = make_map(&m[1], a_lo, args.N, args.K, BM)) != SRWM_OK ||
+        (rc = make_map(&m[2], b_hi, args.Mo, args.K, BN)) != SRWM_OK ||
+        (rc = make_map(&m[3], b_lo, args.Mo, args.K, BN)) != SRWM_OK)
+        return rc;
+    const void* kern = epi == 1 ? reinterpret_cast<const void*>(&ffgemm_kernel<1>)
+                                : reinterpret_cast<const void*>(&ffgemm_kernel<2>);
+    const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    const long long ntiles = static_cast<long long>((args.N + BM - 1) / BM) * ((args.Mo + BN - 1) / BN);
+    const unsigned grid = static_cast<unsigned>(ntiles < n_sm ? ntiles : n_sm);
+    void* kargs[] = {&m[0], &m[1], &m[2], &m[3], const_cast<GemmArgs*>(&args)};
+    if (cudaLaunchKernel(kern, dim3(grid), dim3(NTHREADS), kargs, static_cast<size_t>(smem), st) != cudaSuccess) {
+        cudaGetLastError();
+        return SRWM_ERR_CUDA;
+    }
+    return SRWM_OK;
+}
+
+}  // namespace srwm

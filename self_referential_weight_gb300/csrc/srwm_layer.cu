@@ -8,10 +8,13 @@
 //   a   = LN1(u)                       (this file: ln_kernel)
 //   y   = SRWM(a)                      (the recurrence kernels; heads = d-wide slices of a)
 //   h   = u + y;  b = LN2(h)           (ln_kernel with the residual add fused)
-//   f   = ReLU(b W1^T + b1)            (cuBLASLt, fp32, bias + ReLU epilogue)
-//   out = h + f W2^T + b2              (cuBLASLt, fp32, bias epilogue, accumulating onto h)
-// The two feed-forward products are plain dense GEMMs and go to the library;
-// everything else runs in this library's kernels.
+//   f   = ReLU(b W1^T + b1)            (tensor cores, srwm_ffgemm.cu: bias + ReLU epilogue)
+//   out = h + f W2^T + b2              (tensor cores: bias epilogue, accumulating onto h)
+// The two products run on the tcgen05 tensor cores with fp32 operands split
+// into bf16 (hi, lo) pairs (three products, fp32 accumulation): LN2 writes its
+// output as such a pair, the first product's epilogue writes f as one, and the
+// weights are split at the start of the call.  cuBLASLt stays only as a
+// comparison (srwm_debug_set_layer_gemm).
 #include <cublasLt.h>
 #include <cuda_runtime.h>
 
@@ -21,7 +24,10 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda_bf16.h>
+
 #include "srwm.h"
+#include "srwm_ffgemm.h"
 
 namespace {
 
@@ -35,11 +41,14 @@ size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 // optionally h_out = v; out = (v - mean) / sqrt(var + eps) * g + beta, with
 // the mean and the variance (of deviations from the mean) as fixed-order warp
 // sums, so the result is deterministic.
-template <bool RESIDUAL>
+// SPLIT: the normalised row goes out as bf16 (hi, lo) parts (out_hi, out_lo,
+// x ~ hi + lo) for the tensor-core product that reads it, instead of fp32 out.
+template <bool RESIDUAL, bool SPLIT = false>
 __global__ void __launch_bounds__(256) ln_kernel(const float* __restrict__ a, const float* __restrict__ r,
                                                  float* __restrict__ h_out, const float* __restrict__ g,
                                                  const float* __restrict__ beta, float* __restrict__ out,
-                                                 long long rows, int D)
+                                                 long long rows, int D, __nv_bfloat16* __restrict__ out_hi = nullptr,
+                                                 __nv_bfloat16* __restrict__ out_lo = nullptr)
 {
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -91,19 +100,34 @@ __global__ void __launch_bounds__(256) ln_kernel(const float* __restrict__ a, co
             o4.y = (v[k].y - mean) * rstd * gg.y + bb.y;
             o4.z = (v[k].z - mean) * rstd * gg.z + bb.z;
             o4.w = (v[k].w - mean) * rstd * gg.w + bb.w;
-            reinterpret_cast<float4*>(out + row * D)[q] = o4;
+            if constexpr (SPLIT) {
+                const __nv_bfloat16 hx = __float2bfloat16_rn(o4.x), hy = __float2bfloat16_rn(o4.y);
+                const __nv_bfloat16 hz = __float2bfloat16_rn(o4.z), hw = __float2bfloat16_rn(o4.w);
+                __nv_bfloat162 h2[2] = {__halves2bfloat162(hx, hy), __halves2bfloat162(hz, hw)};
+                __nv_bfloat162 l2[2] = {
+                    __floats2bfloat162_rn(o4.x - __bfloat162float(hx), o4.y - __bfloat162float(hy)),
+                    __floats2bfloat162_rn(o4.z - __bfloat162float(hz), o4.w - __bfloat162float(hw))};
+                reinterpret_cast<uint2*>(out_hi + row * D)[q] = *reinterpret_cast<const uint2*>(h2);
+                reinterpret_cast<uint2*>(out_lo + row * D)[q] = *reinterpret_cast<const uint2*>(l2);
+            } else {
+                reinterpret_cast<float4*>(out + row * D)[q] = o4;
+            }
         }
     }
 }
 
 int launch_ln(bool residual, const float* a, const float* r, float* h_out, const float* g, const float* beta,
-              float* out, long long rows, int D, cudaStream_t st)
+              float* out, long long rows, int D, cudaStream_t st, void* out_hi = nullptr, void* out_lo = nullptr)
 {
     if (rows == 0) return SRWM_OK;
     const int warps = 8;
     const long long blocks = (rows + warps - 1) / warps;
     if (blocks > 0x7fffffffLL) return SRWM_ERR_SHAPE;
-    if (residual)
+    if (residual && out_hi)
+        ln_kernel<true, true><<<static_cast<unsigned>(blocks), 32 * warps, 0, st>>>(
+            a, r, h_out, g, beta, nullptr, rows, D, static_cast<__nv_bfloat16*>(out_hi),
+            static_cast<__nv_bfloat16*>(out_lo));
+    else if (residual)
         ln_kernel<true><<<static_cast<unsigned>(blocks), 32 * warps, 0, st>>>(a, r, h_out, g, beta, out, rows, D);
     else
         ln_kernel<false><<<static_cast<unsigned>(blocks), 32 * warps, 0, st>>>(a, r, h_out, g, beta, out, rows, D);
@@ -113,7 +137,7 @@ int launch_ln(bool residual, const float* a, const float* r, float* h_out, const
 // ---------------------------------------------------------------- cuBLASLt
 constexpr int kMaxDevices = 64;
 cublasLtHandle_t g_lt[kMaxDevices];
-std::atomic<int> g_gemm_mode{0};   // 0: emulated FP32 where offered, 1: plain FP32 only
+std::atomic<int> g_gemm_mode{0};   // 0: tensor cores (this library); 1: cuBLASLt plain FP32; 2: cuBLASLt emulated FP32
 std::mutex g_lt_mu;
 
 int lt_handle(cublasLtHandle_t* out)
@@ -184,16 +208,15 @@ int linear_with(cublasLtHandle_t lt, cublasComputeType_t compute, const float* X
     return SRWM_OK;
 }
 
-// fp32 GEMM: unless plain FP32 is forced (srwm_debug_set_layer_gemm), first as FP32 emulated on the BF16 tensor cores (each fp32
-// input split into three BF16 parts, the nine partial products accumulated in
-// fp32: fp32-level accuracy), else, where cuBLASLt offers no such algorithm
-// for this shape and epilogue, in plain FP32.
+// cuBLASLt fp32 GEMM, for comparison only (srwm_debug_set_layer_gemm): mode 2
+// as FP32 emulated on the BF16 tensor cores (three BF16 parts per input, nine
+// products) where cuBLASLt offers it, mode 1 (or no such algorithm) plain FP32.
 int linear(cublasLtHandle_t lt, const float* X, const float* W, const float* bias, float* out, long long N, int K,
            int M, bool relu, bool accumulate, void* ws, size_t ws_bytes, cudaStream_t st)
 {
     if (N == 0) return SRWM_OK;
     int rc = SRWM_ERR_UNSUPPORTED;
-    if (g_gemm_mode == 0)
+    if (g_gemm_mode == 2)
         rc = linear_with(lt, CUBLAS_COMPUTE_32F_EMULATED_16BFX9, X, W, bias, out, N, K, M, relu, accumulate, ws,
                          ws_bytes, st);
     if (rc == SRWM_ERR_UNSUPPORTED)
@@ -211,12 +234,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 }
 
 struct LayerWs {
-    size_t a, y, f, wf, cnt, lt, total;
+    size_t a, y, f, wf, cnt, w1, w2, lt, total;
 };
 
-// Workspace regions (each 256-byte aligned): a = LN1(u), later LN2(h);
-// y = SRWM output; f = feed-forward hidden; the SRWM's final state and
-// schedule counters; cuBLASLt scratch.
+// Workspace regions (each 256-byte aligned): a = LN1(u), later LN2(h) as a
+// bf16 (hi, lo) pair in the same bytes; y = SRWM output; f = feed-forward
+// hidden (a bf16 pair, or fp32 on the comparison path); the SRWM's final state
+// and schedule counters; W1 and W2 as bf16 pairs; cuBLASLt scratch (comparison
+// path only).
 bool layer_ws(long long B, long long T, long long H, long long d, long long n_lr, long long d_ff, LayerWs* w)
 {
     const long long N = B * T, D = H * d, m = 3 * d + n_lr;
@@ -226,7 +251,9 @@ bool layer_ws(long long B, long long T, long long H, long long d, long long n_lr
     w->f = w->y + align256(static_cast<size_t>(N * D) * 4);
     w->wf = w->f + align256(static_cast<size_t>(N * d_ff) * 4);
     w->cnt = w->wf + align256(static_cast<size_t>(B * H * m * d) * 4);
-    w->lt = w->cnt + align256(static_cast<size_t>(B * H) * 4);
+    w->w1 = w->cnt + align256(static_cast<size_t>(B * H) * 4);
+    w->w2 = w->w1 + align256(static_cast<size_t>(d_ff * D) * 4);
+    w->lt = w->w2 + align256(static_cast<size_t>(d_ff * D) * 4);
     w->total = w->lt + kLtWorkspace;
     return true;
 }
@@ -249,7 +276,7 @@ extern "C" {
 size_t srwm_layer_workspace_bytes(int B, int T, int H, int d, int n_lr, int d_ff)
 {
     if (B <= 0 || T < 0 || H <= 0 || (d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4) || d_ff <= 0 ||
-        d_ff % 4 != 0 || static_cast<long long>(H) * d > 1024)
+        d_ff % 8 != 0 || static_cast<long long>(H) * d > 1024)
         return 0;
     LayerWs w;
     if (!layer_ws(B, T, H, d, n_lr, d_ff, &w)) return 0;
@@ -267,7 +294,7 @@ int srwm_layer_forward(const float* u, int B, int T, int H, int d, int n_lr, int
         return SRWM_ERR_NULL;
     if (B <= 0 || H <= 0 || T < 0 || d_ff <= 0) return SRWM_ERR_SHAPE;
     if ((d != 16 && d != 32 && d != 64) || (n_lr != 1 && n_lr != 4) || (softmax_input != 0 && softmax_input != 1) ||
-        d_ff % 4 != 0 || static_cast<long long>(H) * d > 1024)
+        d_ff % 8 != 0 || static_cast<long long>(H) * d > 1024)
         return SRWM_ERR_UNSUPPORTED;
     LayerWs w;
     if (!layer_ws(B, T, H, d, n_lr, d_ff, &w)) return SRWM_ERR_SHAPE;
@@ -313,19 +340,56 @@ int srwm_layer_forward(const float* u, int B, int T, int H, int d, int n_lr, int
                                     cnt, static_cast<size_t>(B) * H * 4, stream)) != SRWM_OK)
         return rc;
     if (T == 0) return SRWM_OK;
-    // h = u + y goes to out (the second product accumulates onto it); LN2(h) reuses a
-    if ((rc = launch_ln(true, u, y, out, ln2_gamma, ln2_beta, a, N, static_cast<int>(D), st)) != SRWM_OK) return rc;
-    cublasLtHandle_t lt;
-    if ((rc = lt_handle(&lt)) != SRWM_OK) return rc;
-    if ((rc = linear(lt, a, W1, b1, f, N, static_cast<int>(D), d_ff, true, false, ltws, kLtWorkspace, st)) != SRWM_OK)
+    if (g_gemm_mode != 0) {
+        // comparison path: LN2 in fp32 and the two products on cuBLASLt
+        if ((rc = launch_ln(true, u, y, out, ln2_gamma, ln2_beta, a, N, static_cast<int>(D), st)) != SRWM_OK)
+            return rc;
+        cublasLtHandle_t lt;
+        if ((rc = lt_handle(&lt)) != SRWM_OK) return rc;
+        if ((rc = linear(lt, a, W1, b1, f, N, static_cast<int>(D), d_ff, true, false, ltws, kLtWorkspace, st)) !=
+            SRWM_OK)
+            return rc;
+        return linear(lt, f, W2, b2, out, N, d_ff, static_cast<int>(D), false, true, ltws, kLtWorkspace, st);
+    }
+    // h = u + y goes to out (the second product accumulates onto it); LN2(h)
+    // goes out as a bf16 (hi, lo) pair into a's bytes
+    const size_t nND = static_cast<size_t>(N * D), nFD = static_cast<size_t>(d_ff) * static_cast<size_t>(D);
+    __nv_bfloat16* a_hi = reinterpret_cast<__nv_bfloat16*>(a);
+    __nv_bfloat16* a_lo = a_hi + nND;
+    __nv_bfloat16* f_hi = reinterpret_cast<__nv_bfloat16*>(f);
+    __nv_bfloat16* f_lo = f_hi + static_cast<size_t>(N) * d_ff;
+    __nv_bfloat16* w1_hi = reinterpret_cast<__nv_bfloat16*>(base + w.w1);
+    __nv_bfloat16* w1_lo = w1_hi + nFD;
+    __nv_bfloat16* w2_hi = reinterpret_cast<__nv_bfloat16*>(base + w.w2);
+    __nv_bfloat16* w2_lo = w2_hi + nFD;
+    if ((rc = launch_ln(true, u, y, out, ln2_gamma, ln2_beta, nullptr, N, static_cast<int>(D), st, a_hi, a_lo)) !=
+        SRWM_OK)
         return rc;
-    return linear(lt, f, W2, b2, out, N, d_ff, static_cast<int>(D), false, true, ltws, kLtWorkspace, st);
+    if ((rc = srwm::ff_split(W1, w1_hi, w1_lo, static_cast<long long>(nFD), st)) != SRWM_OK ||
+        (rc = srwm::ff_split(W2, w2_hi, w2_lo, static_cast<long long>(nFD), st)) != SRWM_OK)
+        return rc;
+    srwm::GemmArgs ga{};
+    if ((rc = srwm::device_status_ptr(&ga.status)) != SRWM_OK) return rc;
+    ga.wait_limit_ns = srwm::device_wait_limit_ns();
+    ga.N = N;
+    ga.K = static_cast<int>(D);
+    ga.Mo = d_ff;
+    ga.bias = b1;
+    ga.out_hi = f_hi;
+    ga.out_lo = f_lo;
+    if ((rc = srwm::ff_gemm(1, a_hi, a_lo, w1_hi, w1_lo, ga, st)) != SRWM_OK) return rc;
+    ga.K = d_ff;
+    ga.Mo = static_cast<int>(D);
+    ga.bias = b2;
+    ga.out = out;
+    ga.out_hi = ga.out_lo = nullptr;
+    return srwm::ff_gemm(2, f_hi, f_lo, w2_hi, w2_lo, ga, st);
 }
 
-int srwm_debug_set_layer_gemm(int plain_fp32)
+int srwm_debug_set_layer_gemm(int mode)
 {
-    if (plain_fp32 != 0 && plain_fp32 != 1) return SRWM_ERR_UNSUPPORTED;
-    g_gemm_mode.store(plain_fp32);
+    if (mode < 0 || mode > 2) return SRWM_ERR_UNSUPPORTED;
+    g_gemm_mode.store(mode);
     return SRWM_OK;
 }
 
