@@ -35,7 +35,9 @@
  *       * srwm_forward_host's two copy streams and twelve events, created on
  *         its first call on each device;
  *       * srwm_layer_forward's cuBLASLt handle, created by cublasLtCreate
- *         (which allocates) on its first call on each device.
+ *         (which allocates) on the first call on a device that takes the
+ *         cuBLASLt comparison path (srwm_debug_set_layer_gemm 1 or 2); the
+ *         default path does not use cuBLASLt.
  *     The cached addresses and handles belong to the device's primary context:
  *     after cudaDeviceReset on a device, do not call the library on that
  *     device again in the same process.
@@ -262,10 +264,12 @@ size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr);
  *   a = LN1(u);  y = SRWM(a) (as srwm_forward, heads = d-wide slices);
  *   h = u + y;   out = h + W2 ReLU(W1 LN2(h) + b1) + b2
  * LN(v) = (v - mean(v)) / sqrt(var(v) + 1e-5) * gamma + beta over the D
- * entries of a token (biased variance).  Everything is fp32; the two
- * feed-forward products are cuBLASLt GEMMs with fp32 inputs and outputs
- * (FP32 emulated on the BF16 tensor cores where offered, see
- * srwm_debug_set_layer_gemm), the rest runs in this library's kernels.
+ * entries of a token (biased variance).  Inputs, outputs and every stored
+ * value are fp32.  The two feed-forward products run on the tensor cores in
+ * this library's tcgen05 kernel with fp32 operands split into bf16 (hi, lo)
+ * pairs: X W^T ~ X_hi W_hi^T + X_hi W_lo^T + X_lo W_hi^T accumulated in fp32
+ * (about 1e-5 relative error on the products); everything else runs in fp32.
+ * d_ff must be a multiple of 8.
  *
  *   u          [B, T, D]      input tokens
  *   ln*_gamma, ln*_beta [D]   layer-norm scale and shift
@@ -291,12 +295,13 @@ int srwm_layer_forward(const float* u, int B, int T, int H, int d, int n_lr, int
 size_t srwm_layer_workspace_bytes(int B, int T, int H, int d, int n_lr, int d_ff);
 
 /*
- * srwm_debug_set_layer_gemm -- how srwm_layer_forward's feed-forward GEMMs
- * compute: 0 (default) FP32 emulated on the BF16 tensor cores where cuBLASLt
- * offers it (fp32-level accuracy), else plain FP32; 1 plain FP32 only.  For
- * comparisons; applies to calls made afterwards.
+ * srwm_debug_set_layer_gemm -- how srwm_layer_forward's feed-forward products
+ * compute: 0 (default) this library's tensor-core kernel; 1 cuBLASLt plain
+ * FP32; 2 cuBLASLt FP32 emulated on the BF16 tensor cores where it offers
+ * that (else plain FP32).  Modes 1 and 2 exist for comparison; applies to
+ * calls made afterwards.  SRWM_ERR_UNSUPPORTED for any other mode.
  */
-int srwm_debug_set_layer_gemm(int plain_fp32);
+int srwm_debug_set_layer_gemm(int mode);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* srwm_status_string(int status);

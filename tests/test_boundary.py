@@ -220,3 +220,11 @@ def test_layer_workspace_and_validation(lib):
     assert call(ws_bytes=1024) == 2
     assert call(out=base + 0xA0004) == 4
     assert call(out=base) == 5                          # out over u
+
+
+def test_layer_gemm_mode_is_checked(lib):
+    lib.srwm_debug_set_layer_gemm.argtypes = [ctypes.c_int]
+    lib.srwm_debug_set_layer_gemm.restype = ctypes.c_int
+    assert lib.srwm_debug_set_layer_gemm(3) == 3    # SRWM_ERR_UNSUPPORTED
+    assert lib.srwm_debug_set_layer_gemm(-1) == 3
+    assert lib.srwm_debug_set_layer_gemm(0) == 0

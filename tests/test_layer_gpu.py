@@ -72,3 +72,22 @@ def test_layer_zero_steps_returns_W0():
     u = np.zeros((3, 0, H * d), np.float32)
     _, Wf = run_layer(u, H, 4, False, p)
     np.testing.assert_array_equal(Wf, np.broadcast_to(p["W0"], Wf.shape))
+
+
+def test_layer_tensor_core_products_agree_with_cublaslt():
+    """The default path (this library's tensor-core kernel, bf16 (hi, lo)
+    operand pairs) against the cuBLASLt plain-FP32 comparison path and the
+    oracle, on the wide shape (D = 512, d_ff = 2048: K = 512 and 2048)."""
+    B, T, H, d, n_lr = 16, 40, 8, 64, 4
+    p = inputs.make_layer_params(H, d, n_lr, 4 * H * d, 240)
+    u = inputs.make_layer_input(B, T, H * d, 240)
+    tc, _ = run_layer(u, H, n_lr, False, p)
+    binding.srwm_debug_set_layer_gemm(1)
+    try:
+        ref, _ = run_layer(u, H, n_lr, False, p)
+    finally:
+        binding.srwm_debug_set_layer_gemm(0)
+    oo, _ = srwm_layer.layer_forward(u, H, n_lr, False, p)
+    e_tc, e_ref, e_vs = rel(tc, oo), rel(ref, oo), rel(tc, ref)
+    print(f"layer out vs oracle: tensor cores {e_tc:.2e}, cuBLASLt FP32 {e_ref:.2e}; between them {e_vs:.2e}")
+    assert e_tc <= 1e-4 and e_ref <= 1e-4 and e_vs <= 1e-4
