@@ -228,3 +228,10 @@ def test_layer_gemm_mode_is_checked(lib):
     assert lib.srwm_debug_set_layer_gemm(3) == 3    # SRWM_ERR_UNSUPPORTED
     assert lib.srwm_debug_set_layer_gemm(-1) == 3
     assert lib.srwm_debug_set_layer_gemm(0) == 0
+
+
+def test_layer_hidden_width_must_be_a_multiple_of_8(lib):
+    lib.srwm_layer_workspace_bytes.argtypes = [ctypes.c_int] * 6
+    lib.srwm_layer_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.srwm_layer_workspace_bytes(2, 8, 2, 16, 4, 64) > 0
+    assert lib.srwm_layer_workspace_bytes(2, 8, 2, 16, 4, 12) == 0

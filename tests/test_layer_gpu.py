@@ -91,3 +91,17 @@ def test_layer_tensor_core_products_agree_with_cublaslt():
     e_tc, e_ref, e_vs = rel(tc, oo), rel(ref, oo), rel(tc, ref)
     print(f"layer out vs oracle: tensor cores {e_tc:.2e}, cuBLASLt FP32 {e_ref:.2e}; between them {e_vs:.2e}")
     assert e_tc <= 1e-4 and e_ref <= 1e-4 and e_vs <= 1e-4
+
+
+@pytest.mark.parametrize("B,T,H,d,d_ff", [(1, 1, 2, 16, 8), (3, 45, 8, 64, 2048), (2, 33, 2, 32, 24),
+                                          (1, 129, 4, 16, 64)])
+def test_layer_tile_edges(B, T, H, d, d_ff):
+    """Shapes at the tensor-core products' tile edges: one token, token
+    counts off the 128-row tiles, hidden widths below one 256-column tile
+    and inner dimensions below one 64-wide K step (filled with zeros by TMA)."""
+    n_lr = 4
+    p = inputs.make_layer_params(H, d, n_lr, d_ff, 250 + T)
+    u = inputs.make_layer_input(B, T, H * d, 250 + T)
+    out, _ = run_layer(u, H, n_lr, False, p)
+    oo, _ = srwm_layer.layer_forward(u, H, n_lr, False, p)
+    assert rel(out, oo) <= 1e-4, rel(out, oo)
