@@ -17,12 +17,16 @@
 // Persistent, warp-specialised CTA (one per SM): warp 0 issues the TMA loads,
 // warp 1 the MMAs (one thread each), warps 2-5 run the epilogue, each on the
 // 32 tensor-memory lanes (= tile rows) its warp may access.  Tiles of 128 x 256
-// outputs; K in steps of 64 (one 128-byte swizzle row of bf16); two shared-
-// memory stages (A_hi, A_lo, B_hi, B_lo: 96 KB each) and two accumulators in
+// outputs; K in steps of 32 (one 64-byte swizzle row of bf16); four shared-
+// memory stages (A_hi, A_lo, B_hi, B_lo: 48 KB each) and two accumulators in
 // tensor memory (2 x 256 columns), so one tile's epilogue overlaps the next
-// tile's products.  Every wait is bounded; a timeout sets the status word,
-// stops new work, waits (bounded) for work in flight and frees the tensor
-// memory.
+// tile's products.  The epilogue stages each warp's 32 x 32 blocks in shared
+// memory (two buffers per warp) and writes them with TMA: a store of the bf16
+// pair (1), a reduce-add onto out (2).  Tensor memory holds one tile row per
+// lane, so direct stores from registers would scatter every instruction over
+// 32 rows; they made the epilogue the products' limit.  Every wait is
+// bounded; a timeout sets the status word, stops new work, waits (bounded)
+// for work in flight and frees the tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,21 +43,23 @@
 namespace srwm {
 namespace ff {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 2, NACC = 2;
-constexpr int TILE_A = BM * BK * 2;                    // bytes of one bf16 A tile (16 KB)
-constexpr int TILE_B = BN * BK * 2;                    // 32 KB
+constexpr int BM = 128, BN = 256, BK = 32, STAGES = 4, NACC = 2;
+constexpr int TILE_A = BM * BK * 2;                    // bytes of one bf16 A tile (8 KB)
+constexpr int TILE_B = BN * BK * 2;                    // 16 KB
 constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;   // A_hi | A_lo | B_hi | B_lo
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = NACC * BN;              // 512: the whole tensor memory of the SM
+constexpr int OBUF = 32 * 32 * 4;                      // one 32 x 32 output block: fp32, or the bf16 pair
 
 struct __align__(1024) Smem {
     uint8_t stage[STAGES][STAGE_BYTES];
+    uint8_t ostage[4][2][OBUF];                        // per epilogue warp, two blocks in flight
     uint64_t full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC];
     uint32_t tmem_base;
     int abort;
 };
 static_assert(STAGE_BYTES % 1024 == 0 && TILE_A % 1024 == 0 && TILE_B % 1024 == 0,
-              "128-byte swizzled tiles start on 1024-byte boundaries");
+              "swizzled tiles start on 1024-byte boundaries");
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
 {
@@ -64,22 +70,42 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// TMA store of a 2-D box shared -> global (bulk group), and the reduce-add form
+// (global += box, element type from the map)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_add_2d(const CUtensorMap* map, const void* src, int c0, int c1)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// the 128-byte swizzle: rows of 128 bytes (64 bf16 along K), atoms of 8 rows
-// (1024 bytes, the stride between 8-row groups); the leading-dimension offset
+// the 64-byte swizzle: rows of 64 bytes (32 bf16 along K), atoms of 8 rows
+// (512 bytes, the stride between 8-row groups); the leading-dimension offset
 // is not used by this layout.  Bits: start address >> 4 [0, 14), leading byte
 // offset >> 4 [16, 30), stride byte offset >> 4 [32, 46), descriptor version 1
-// [46, 48), swizzle mode [61, 64) (2: 128-byte).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+// [46, 48), swizzle mode [61, 64) (4: 64-byte).  (K steps of 64 with the
+// 128-byte swizzle and two 96 KB stages were ~7 % slower on the layer's
+// products: half as many stages in flight.)
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr)
 {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
+           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(4) << 61);
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
@@ -140,6 +166,7 @@ template <int EPI>
 __global__ void __launch_bounds__(NTHREADS, 1)
     ffgemm_kernel(const __grid_constant__ CUtensorMap ta_hi, const __grid_constant__ CUtensorMap ta_lo,
                   const __grid_constant__ CUtensorMap tb_hi, const __grid_constant__ CUtensorMap tb_lo,
+                  const __grid_constant__ CUtensorMap to0, const __grid_constant__ CUtensorMap to1,
                   const GemmArgs ga)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -168,6 +195,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         prefetch_tensormap(&ta_lo);
         prefetch_tensormap(&tb_hi);
         prefetch_tensormap(&tb_lo);
+        prefetch_tensormap(&to0);
+        if (EPI == 1) prefetch_tensormap(&to1);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -244,9 +273,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint32_t ko = static_cast<uint32_t>(k * 32);   // 16 bf16 along K
-                    const uint64_t a_hi = sw128_desc(base + ko), a_lo = sw128_desc(base + TILE_A + ko);
-                    const uint64_t b_hi = sw128_desc(base + 2 * TILE_A + ko);
-                    const uint64_t b_lo = sw128_desc(base + 2 * TILE_A + TILE_B + ko);
+                    const uint64_t a_hi = sw64_desc(base + ko), a_lo = sw64_desc(base + TILE_A + ko);
+                    const uint64_t b_hi = sw64_desc(base + 2 * TILE_A + ko);
+                    const uint64_t b_lo = sw64_desc(base + 2 * TILE_A + TILE_B + ko);
                     umma(d, a_hi, b_hi, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma(d, a_hi, b_lo, idesc, 1u);
                     umma(d, a_lo, b_hi, idesc, 1u);
@@ -268,9 +297,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
     } else {
-        // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31,
+        // i.e. tile rows 32 (w % 4) .., 32 columns at a time; each 32 x 32
+        // block goes through the warp's staging buffers to a TMA store
         const int q = warp & 3;
-        int li = 0;
+        int li = 0, nb = 0;   // tiles, blocks staged so far
         for (int tile = blockIdx.x; tile < ntiles && !*abort; tile += gridDim.x, ++li) {
             const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
             const int ab = li & 1;
@@ -280,47 +311,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc_fence_after();
-            const long long row = m0 + 32 * q + lane;
-            const bool row_ok = row < ga.N;
+            const int r0 = m0 + 32 * q;   // first row of this warp's blocks
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = n0 + 32 * c;
                 uint32_t r[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 32 * c), r);
-                if (col0 >= ga.Mo) continue;
+                if (c == BN / 32 - 1) {
+                    // the accumulator may take the next tile
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);
+                }
+                if (col0 >= ga.Mo || r0 >= ga.N) continue;
+                float v[32];
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {   // 8 columns at a time
-                    const int cc = col0 + 8 * g;
-                    if (!row_ok || cc >= ga.Mo) continue;
-                    float v[8];
-                    const float4 b0 = __ldg(reinterpret_cast<const float4*>(ga.bias + cc));
-                    const float4 b1 = __ldg(reinterpret_cast<const float4*>(ga.bias + cc + 4));
-                    const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                for (int k = 0; k < 8; ++k) {   // bias of columns col0 + 4k .. (zero past the output's width)
+                    const float4 b4 = col0 + 4 * k < ga.Mo ? __ldg(reinterpret_cast<const float4*>(ga.bias + col0 + 4 * k))
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[4 * k] = __uint_as_float(r[4 * k]) + b4.x;
+                    v[4 * k + 1] = __uint_as_float(r[4 * k + 1]) + b4.y;
+                    v[4 * k + 2] = __uint_as_float(r[4 * k + 2]) + b4.z;
+                    v[4 * k + 3] = __uint_as_float(r[4 * k + 3]) + b4.w;
+                }
+                uint8_t* buf = sm.ostage[q][nb & 1];
+                // the store that read this buffer two blocks ago is done with it
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                if constexpr (EPI == 1) {
+                    // row `lane` of the hi block (64 bytes) and of the lo block
+                    uint4* hrow = reinterpret_cast<uint4*>(buf + 64 * lane);
+                    uint4* lrow = reinterpret_cast<uint4*>(buf + 2048 + 64 * lane);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[8 * g + j]) + bb[j];
-                    if constexpr (EPI == 1) {
+                    for (int k = 0; k < 4; ++k) {
                         float hi[8], lo[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) split_bf16(fmaxf(v[j], 0.f), hi[j], lo[j]);
-                        const size_t o = static_cast<size_t>(row) * ga.Mo + cc;
-                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ga.out_hi) + o) =
-                            make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]),
-                                       pack_bf16(hi[6], hi[7]));
-                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ga.out_lo) + o) =
-                            make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
-                                       pack_bf16(lo[6], lo[7]));
-                    } else {
-                        float4* o = reinterpret_cast<float4*>(ga.out + static_cast<size_t>(row) * ga.Mo + cc);
-                        const float4 h0 = o[0], h1 = o[1];
-                        o[0] = make_float4(h0.x + v[0], h0.y + v[1], h0.z + v[2], h0.w + v[3]);
-                        o[1] = make_float4(h1.x + v[4], h1.y + v[5], h1.z + v[6], h1.w + v[7]);
+                        for (int j = 0; j < 8; ++j) split_bf16(fmaxf(v[8 * k + j], 0.f), hi[j], lo[j]);
+                        hrow[k] = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]),
+                                             pack_bf16(hi[6], hi[7]));
+                        lrow[k] = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
+                                             pack_bf16(lo[6], lo[7]));
                     }
+                } else {
+                    // row `lane` (128 bytes) in the map's 128-byte swizzle: 16-byte chunk
+                    // k sits at chunk k ^ (row % 8), so the eight lanes of a phase hit
+                    // eight different bank groups
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4*>(buf + 128 * lane + 16 * (k ^ (lane & 7))) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (EPI == 1) {
+                        tma_store_2d(&to0, buf, col0, r0);
+                        tma_store_2d(&to1, buf + 2048, col0, r0);
+                    } else {
+                        tma_add_2d(&to0, buf, col0, r0);
+                    }
+                    bulk_commit();
+                }
+                ++nb;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[ab]);   // the accumulator may take the next tile
         }
+        // the blocks in flight are written before the CTA ends
+        if (lane == 0) bulk_wait_all<0>();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -361,7 +418,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 }
 
 // 2-D map over a row-major bf16 [rows, K] matrix: boxes of `box_rows` rows x
-// 64 columns, 128-byte swizzle, zero fill outside the matrix.
+// 32 columns, 64-byte swizzle, zero fill outside the matrix.
 int make_map(CUtensorMap* map, const void* base, long long rows, int K, int box_rows)
 {
     auto enc = encoder();
@@ -371,8 +428,26 @@ int make_map(CUtensorMap* map, const void* base, long long rows, int K, int box_
     cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
+}
+
+// 2-D map over a row-major [rows, cols] output (bf16 or fp32) in boxes of 32 x 32,
+// the 128-byte swizzle for fp32 (a box row is 128 bytes), none for bf16.
+int make_out_map(CUtensorMap* map, void* base, long long rows, int cols, bool fp32)
+{
+    auto enc = encoder();
+    if (!enc) return SRWM_ERR_CUDA;
+    const int es = fp32 ? 4 : 2;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
 }
 
@@ -393,13 +468,21 @@ int ff_gemm(int epi, const void* a_hi, const void* a_lo, const void* b_hi, const
     using namespace ff;
     if (args.N <= 0 || args.Mo <= 0) return SRWM_OK;
     if (args.K <= 0 || args.K % 8 != 0 || args.Mo % 8 != 0) return SRWM_ERR_UNSUPPORTED;
-    CUtensorMap m[4];
+    CUtensorMap m[6];
     int rc;
     if ((rc = make_map(&m[0], a_hi, args.N, args.K, BM)) != SRWM_OK ||
         (rc = make_map(&m[1], a_lo, args.N, args.K, BM)) != SRWM_OK ||
         (rc = make_map(&m[2], b_hi, args.Mo, args.K, BN)) != SRWM_OK ||
         (rc = make_map(&m[3], b_lo, args.Mo, args.K, BN)) != SRWM_OK)
         return rc;
+    if (epi == 1) {
+        if ((rc = make_out_map(&m[4], args.out_hi, args.N, args.Mo, false)) != SRWM_OK ||
+            (rc = make_out_map(&m[5], args.out_lo, args.N, args.Mo, false)) != SRWM_OK)
+            return rc;
+    } else {
+        if ((rc = make_out_map(&m[4], args.out, args.N, args.Mo, true)) != SRWM_OK) return rc;
+        m[5] = m[4];
+    }
     const void* kern = epi == 1 ? reinterpret_cast<const void*>(&ffgemm_kernel<1>)
                                 : reinterpret_cast<const void*>(&ffgemm_kernel<2>);
     const int smem = static_cast<int>(sizeof(Smem)) + 1024;
@@ -411,7 +494,7 @@ int ff_gemm(int epi, const void* a_hi, const void* a_lo, const void* b_hi, const
     }
     const long long ntiles = static_cast<long long>((args.N + BM - 1) / BM) * ((args.Mo + BN - 1) / BN);
     const unsigned grid = static_cast<unsigned>(ntiles < n_sm ? ntiles : n_sm);
-    void* kargs[] = {&m[0], &m[1], &m[2], &m[3], const_cast<GemmArgs*>(&args)};
+    void* kargs[] = {&m[0], &m[1], &m[2], &m[3], &m[4], &m[5], const_cast<GemmArgs*>(&args)};
     if (cudaLaunchKernel(kern, dim3(grid), dim3(NTHREADS), kargs, static_cast<size_t>(smem), st) != cudaSuccess) {
         cudaGetLastError();
         return SRWM_ERR_CUDA;
