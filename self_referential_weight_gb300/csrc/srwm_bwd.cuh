@@ -23,8 +23,9 @@
 // subtracts from W exactly the recorded rank-one update the forward added
 // (no matrix inversion, which would amplify rounding wherever the update
 // contracts W), so W_{t-1} is recovered to within a few ulps that grow like
-// sqrt(T).  x~ and dy are staged per KSEG-step segment, together with the
-// segment's records.
+// sqrt(T).  x~, dy and the forward's records are staged per KSEG-step
+// segment by bulk asynchronous copies into one of two buffers, the next
+// segment's while the current one's steps run.
 // Layout: thread (rg = tid/4, cg = tid%4) holds rows rg + RG i (i < S) and the
 // D/4 columns of float4 chunks cg + 4 j.  Row dot products finish with two xor
 // shuffles over the four column groups; column sums over rows finish with a
@@ -74,22 +75,20 @@ struct BwdCfg {
     static constexpr int MP = S * RG;            // padded rows
     static constexpr int CPT = D / 4;            // columns per thread
     static constexpr int NCH = CPT / 4;          // float4 chunks per thread
-    static constexpr int KSEG = 32;              // steps per segment
+    static constexpr int KSEG = D == 16 ? 16 : 32;   // steps per segment (two buffers of them)
+    static constexpr int RS = emit_record_floats(D, NLR);   // floats per record
     static constexpr int NV2 = 2 * CPT;          // values of a two-vector column reduction
     static constexpr int NV1 = CPT < 8 ? 8 : CPT;  // one-vector reduction (padded to 8)
 };
 
 template <class C>
-struct __align__(16) BwdSmem {
-    float xs[C::KSEG][C::D];   // x~ of the segment's steps
-    float dyv[C::KSEG][C::D];  // dy of the segment's steps
-    float pk[C::KSEG][C::D];
-    float u[C::KSEG][C::D];
-    float a[C::KSEG][C::MP];
-    float g[C::KSEG][4];
-    float z[C::MP];
-    float dz[C::MP];
-    float dgrow[C::MP];
+struct __align__(128) BwdSmem {
+    // a segment's steps, by buffer: the forward's records as written
+    // ([phi(k) | u | gates | a], KParams::emit layout), x~ and dy
+    float rec[2][C::KSEG][C::RS];
+    float xs[2][C::KSEG][C::D];
+    float dyv[2][C::KSEG][C::D];
+    uint64_t bar[2];             // "segment landed", by buffer
     float red[C::NW][2][C::D];   // per-warp column partials
     float vec[2][C::D];          // column sums
     float bred[C::NW][4];        // per-warp block sums of dcoef a
@@ -202,19 +201,49 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                     make_float4(m[i][2 * j].x, m[i][2 * j].y, m[i][2 * j + 1].x, m[i][2 * j + 1].y);
         }
     };
-    // x~ (and optionally dy) of steps t0 .. t0+len-1 into shared memory
-    auto stage = [&](int t0, int len, bool with_dy) {
-        constexpr int Q = D / 4;
-        for (int idx = tid; idx < len * Q; idx += C::NT) {
-            const int s = idx / Q, c = 4 * (idx - s * Q);
-            const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D + c;
-            *reinterpret_cast<float4*>(&sm.xs[s][c]) = __ldg(reinterpret_cast<const float4*>(bp.x + g));
-            if (with_dy) *reinterpret_cast<float4*>(&sm.dyv[s][c]) = __ldg(reinterpret_cast<const float4*>(bp.dy + g));
+    // ---- segment staging: one thread per row issues bulk copies of x and dy
+    // rows, lane 0 of warp 0 the segment's records (contiguous per stream) and
+    // the expected byte count; completion on sm.bar[buffer]
+    if (tid == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int n_issued = 0, n_used = 0;   // segments issued / consumed by this CTA (buffer = count % 2)
+    bool in_flight[2] = {false, false};
+    auto issue = [&](int t0, int len) {
+        const int buf = n_issued & 1;
+        ++n_issued;
+        in_flight[buf] = true;
+        if (warp != 0) return;
+        const uint32_t row_bytes = D * 4, rec_bytes = static_cast<uint32_t>(len) * C::RS * 4;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.bar[buf], 2 * len * row_bytes + rec_bytes);
+            bulk_load(&sm.rec[buf][0][0], bp.rec + (static_cast<size_t>(p) * T + t0) * C::RS, rec_bytes, &sm.bar[buf]);
         }
-        __syncthreads();
-        if (softmax_input) {
-            for (int s = warp; s < len; s += C::NW) warp_softmax<D>(sm.xs[s], sm.xs[s], lane);
-            __syncthreads();
+        for (int s = lane; s < len; s += 32) {
+            const size_t g = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
+            bulk_load(&sm.xs[buf][s][0], bp.x + g, row_bytes, &sm.bar[buf]);
+            bulk_load(&sm.dyv[buf][s][0], bp.dy + g, row_bytes, &sm.bar[buf]);
+        }
+    };
+    // waits (bounded) for the next issued segment; false on a timeout (every
+    // thread agrees)
+    auto land = [&]() -> bool {
+        const int buf = n_used & 1;
+        const uint32_t par = (n_used >> 1) & 1;
+        const bool ok = mbar_wait_bounded(&sm.bar[buf], par, bp.wait_limit_ns);
+        if (__syncthreads_or(!ok)) return false;
+        in_flight[buf] = false;
+        ++n_used;
+        return true;
+    };
+    // before giving up the shared memory: the copies still in flight land
+    auto drain = [&]() {
+        for (int k = n_used; k < n_issued; ++k) {
+            const int buf = k & 1;
+            if (in_flight[buf]) mbar_wait_bounded(&sm.bar[buf], (k >> 1) & 1, bp.wait_limit_ns);
         }
     };
     // column sums over all rows of per-thread partials v[N] (N/CPT vectors):
@@ -311,6 +340,7 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
             if (tid == 0) fail = !wait_counter_bounded(bp.seg_done + p, seg, bp.wait_limit_ns);
             if (__syncthreads_or(fail)) {
                 if (tid == 0) atomicOr(bp.status, kStatusTimeout);
+                drain();
                 return;
             }
         }
@@ -334,66 +364,46 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
             }
         }
     }
-    // ---- segments backwards; each step subtracts its recorded update from W
+    // ---- segments backwards; each step subtracts its recorded update from W.
+    // The copies into a buffer follow the reads of the segment before last
+    // (the barrier ending a segment) and the proxy fence of every thread.
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (t_hi > t_lo) issue(max(t_lo, t_hi - KSEG), min(KSEG, t_hi - t_lo));
     for (int top = t_hi; top > t_lo; top -= KSEG) {
         const int t0 = max(t_lo, top - KSEG);
         const int len = top - t0;
-        stage(t0, len, true);
-        // the forward's records of the segment: phi(k), u, gates, a.  float4
-        // pieces (every field starts at a multiple of 4 floats), four loads in
-        // flight per thread; a record's tail past row M-1 and the padded rows
-        // up to MP are zeroed.
-        {
-            const int q4 = bp.rec_stride >> 2;   // float4 per record
-            const float4* src = reinterpret_cast<const float4*>(bp.rec + (static_cast<size_t>(p) * T + t0) * bp.rec_stride);
-            const int n4 = len * q4;
-            for (int base = tid; base < n4; base += 4 * C::NT) {
-                float4 v[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int q = base + k * C::NT;
-                    if (q < n4) v[k] = __ldg(src + q);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int q = base + k * C::NT;
-                    if (q >= n4) continue;
-                    const int s = q / q4, e = 4 * (q - s * q4);
-                    if (e < D) {
-                        *reinterpret_cast<float4*>(&sm.pk[s][e]) = v[k];
-                    } else if (e < 2 * D) {
-                        *reinterpret_cast<float4*>(&sm.u[s][e - D]) = v[k];
-                    } else if (e < 2 * D + 4) {
-                        *reinterpret_cast<float4*>(&sm.g[s][0]) = v[k];
-                    } else {
-                        const int r = e - 2 * D - 4;
-                        sm.a[s][r + 0] = r + 0 < M ? v[k].x : 0.f;
-                        sm.a[s][r + 1] = r + 1 < M ? v[k].y : 0.f;
-                        sm.a[s][r + 2] = r + 2 < M ? v[k].z : 0.f;
-                        sm.a[s][r + 3] = r + 3 < M ? v[k].w : 0.f;
-                    }
-                }
-            }
-            constexpr int R0 = (emit_record_floats(D, NLR) - 2 * D - 4);   // rows covered by a record
-            for (int idx = tid; idx < len * (C::MP - R0); idx += C::NT) {
-                const int s = idx / (C::MP - R0);
-                sm.a[s][R0 + idx - s * (C::MP - R0)] = 0.f;
-            }
+        const int buf = n_used & 1;
+        if (!land()) {
+            if (tid == 0) atomicOr(bp.status, kStatusTimeout);
+            drain();
+            return;
         }
-        __syncthreads();
+        if (softmax_input) {
+            for (int s = warp; s < len; s += C::NW) warp_softmax<D>(sm.xs[buf][s], sm.xs[buf][s], lane);
+            fence_proxy_async_smem();
+            __syncthreads();
+        }
+        // the next segment (earlier steps) into the other buffer
+        if (t0 > t_lo) issue(max(t_lo, t0 - KSEG), min(KSEG, t0 - t_lo));
+        const float* rec = &sm.rec[buf][0][0];
+        auto pk_of = [&](int s) { return rec + s * C::RS; };
+        auto u_of = [&](int s) { return rec + s * C::RS + D; };
+        auto g_of = [&](int s, int blkidx) { return rec[s * C::RS + 2 * D + blkidx]; };
+        auto a_of = [&](int s, int r) { return r < M ? rec[s * C::RS + 2 * D + 4 + r] : 0.f; };
         for (int s = len - 1; s >= 0; --s) {
             // 1. step back: W_{t-1} = W_t - coef (outer) pk; dcoef = dW pk
             float av[S], dco[S];
 #pragma unroll
             for (int i = 0; i < S; ++i) {
                 const int r = rg + RG * i;
-                av[i] = sm.a[s][r];
-                const float coef = sm.g[s][gidx(r)] * av[i];
+                av[i] = a_of(s, r);
+                const float coef = g_of(s, gidx(r)) * av[i];
                 const float2 nc = make_float2(-coef, -coef);
                 float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int q = 0; q < CP; ++q) {
-                    const float2 pk2 = *reinterpret_cast<const float2*>(&sm.pk[s][bcol<C>(cg, 2 * q)]);
+                    const float2 pk2 = *reinterpret_cast<const float2*>(pk_of(s) + bcol<C>(cg, 2 * q));
                     w[i][q] = __ffma2_rn(nc, pk2, w[i][q]);
                     acc = __ffma2_rn(dw[i][q], pk2, acc);
                 }
@@ -416,7 +426,7 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
 #pragma unroll
                 for (int i = 0; i < S; ++i) {
                     const int r = rg + RG * i;
-                    const float g = sm.g[s][gidx(r)];
+                    const float g = g_of(s, gidx(r));
                     const float coef = g * av[i];
                     da[i] = g * dco[i];
                     bs[i] = cg == 0 ? dco[i] * av[i] : 0.f;
@@ -448,19 +458,19 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                 const float* v2 = sm.vec[1];
                 float dk = 0.f, dq = 0.f;   // <phi(k), dphi(k)>, <phi(q), dphi(q)>
                 for (int c = lane; c < D; c += 32) {
-                    const float pkc = sm.pk[s][c], pqc = sm.u[s][c] + pkc;
+                    const float pkc = pk_of(s)[c], pqc = u_of(s)[c] + pkc;
                     dk = fmaf(pkc, v1[c] - v2[c], dk);
                     dq = fmaf(pqc, v2[c], dq);
                 }
                 dk = group_sum<32>(dk);
                 dq = group_sum<32>(dq);
-                const float pkr = sm.pk[s][rg], pqr = sm.u[s][rg] + pkr;
-                dz[0] = sm.dyv[s][rg];
+                const float pkr = pk_of(s)[rg], pqr = u_of(s)[rg] + pkr;
+                dz[0] = sm.dyv[buf][s][rg];
                 dz[1] = pkr * ((v1[rg] - v2[rg]) - dk);
                 dz[2] = pqr * (v2[rg] - dq);
                 dz[3] = 0.f;
                 if (rg < NLR) {
-                    const float g = sm.g[s][rg];
+                    const float g = g_of(s, rg);
                     dz[3] = sm.bsum[rg] * g * (1.f - g);
                 }
             }
@@ -476,8 +486,8 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
 #pragma unroll
                     for (int q = 0; q < CP; ++q) {
                         const int c = bcol<C>(cg, 2 * q);
-                        dw[i][q] = __ffma2_rn(dd, *reinterpret_cast<const float2*>(&sm.u[s][c]), dw[i][q]);
-                        dw[i][q] = __ffma2_rn(zz, *reinterpret_cast<const float2*>(&sm.xs[s][c]), dw[i][q]);
+                        dw[i][q] = __ffma2_rn(dd, *reinterpret_cast<const float2*>(u_of(s) + c), dw[i][q]);
+                        dw[i][q] = __ffma2_rn(zz, *reinterpret_cast<const float2*>(&sm.xs[buf][s][c]), dw[i][q]);
                         c3[q] = __ffma2_rn(w[i][q], zz, c3[q]);
                     }
                 }
@@ -498,15 +508,17 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                 if (warp == 0) {
                     const float* dxv = sm.vec[0];
                     float dot = 0.f;
-                    for (int c = lane; c < D; c += 32) dot = fmaf(sm.xs[s][c], dxv[c], dot);
+                    for (int c = lane; c < D; c += 32) dot = fmaf(sm.xs[buf][s][c], dxv[c], dot);
                     dot = group_sum<32>(dot);
-                    for (int c = lane; c < D; c += 32) bp.dx[gx + c] = sm.xs[s][c] * (dxv[c] - dot);
+                    for (int c = lane; c < D; c += 32) bp.dx[gx + c] = sm.xs[buf][s][c] * (dxv[c] - dot);
                 }
             } else if (tid < D) {
                 bp.dx[gx + tid] = sm.vec[0][tid];
             }
         }
-        __syncthreads();   // the segment's staged vectors are read before the next segment's staging
+        // the segment's buffer is read before copies into it (two segments on)
+        fence_proxy_async_smem();
+        __syncthreads();
     }
     store_tile(dw, bp.dW_seq + static_cast<size_t>(p) * MD);
     if (t_lo > 0) {
