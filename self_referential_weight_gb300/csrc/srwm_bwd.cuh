@@ -64,6 +64,16 @@ struct BwdParams {
     unsigned long long wait_limit_ns;  // bounded-wait limit
 };
 
+// Bulk copy of `bytes` global -> shared, completing `bytes` on bar (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 template <int D_, int NLR_>
 struct BwdCfg {
     static constexpr int D = D_, NLR = NLR_;

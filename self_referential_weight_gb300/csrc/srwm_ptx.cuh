@@ -103,16 +103,6 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
         : "memory");
 }
 
-// Bulk copy of `bytes` global -> shared, completing `bytes` on bar (both
-// addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups still read shared memory.
