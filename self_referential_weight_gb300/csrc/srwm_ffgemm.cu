@@ -17,8 +17,9 @@
 // Persistent, warp-specialised CTA (one per SM): warp 0 issues the TMA loads,
 // warp 1 the MMAs (one thread each), warps 2-5 run the epilogue, each on the
 // 32 tensor-memory lanes (= tile rows) its warp may access.  Tiles of 128 x 256
-// outputs; K in steps of 32 (one 64-byte swizzle row of bf16); four shared-
-// memory stages (A_hi, A_lo, B_hi, B_lo: 48 KB each) and two accumulators in
+// outputs; K in steps of 32 (a 64-byte swizzle row of bf16) over four shared-
+// memory stages (A_hi, A_lo, B_hi, B_lo: 48 KB each), or for K <= 1024 in
+// steps of 64 (128-byte swizzle) over two 96 KB stages; two accumulators in
 // tensor memory (2 x 256 columns), so one tile's epilogue overlaps the next
 // tile's products.  The epilogue stages each warp's 32 x 32 blocks in shared
 // memory (two buffers per warp) and writes them with TMA: a store of the bf16
@@ -43,23 +44,37 @@
 namespace srwm {
 namespace ff {
 
-constexpr int BM = 128, BN = 256, BK = 32, STAGES = 4, NACC = 2;
-constexpr int TILE_A = BM * BK * 2;                    // bytes of one bf16 A tile (8 KB)
-constexpr int TILE_B = BN * BK * 2;                    // 16 KB
-constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;   // A_hi | A_lo | B_hi | B_lo
+constexpr int BM = 128, BN = 256, NACC = 2;
 constexpr int NTHREADS = 192;
+
+// K step (bf16 elements per swizzled tile row) and shared-memory stages.  The
+// products of the layer: K = 512 (eight K steps per tile at BK = 64) is ~4 %
+// faster with two 96 KB stages; K = 2048 ~14 % faster with four 48 KB stages
+// (its 64 K steps per tile gain from the deeper pipeline).
+template <int BK_>
+struct Pipe {
+    static constexpr int BK = BK_;
+    static constexpr int STAGES = BK == 64 ? 2 : 4;
+    static constexpr int TILE_A = BM * BK * 2;                    // bytes of one bf16 A tile
+    static constexpr int TILE_B = BN * BK * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_A + 2 * TILE_B;   // A_hi | A_lo | B_hi | B_lo
+    static constexpr int SBO = BK * 2 * 8;                        // bytes between 8-row atoms
+    static constexpr uint64_t SWZ = BK == 64 ? 2 : 4;             // descriptor swizzle mode: 128 / 64 bytes
+    static_assert(BK == 32 || BK == 64, "K steps of 32 or 64");
+    static_assert(STAGE_BYTES % 1024 == 0 && TILE_A % 1024 == 0 && TILE_B % 1024 == 0,
+                  "swizzled tiles start on 1024-byte boundaries");
+};
 constexpr uint32_t TMEM_COLS = NACC * BN;              // 512: the whole tensor memory of the SM
 constexpr int OBUF = 32 * 32 * 4;                      // one 32 x 32 output block: fp32, or the bf16 pair
 
+template <class P>
 struct __align__(1024) Smem {
-    uint8_t stage[STAGES][STAGE_BYTES];
+    uint8_t stage[P::STAGES][P::STAGE_BYTES];
     uint8_t ostage[4][2][OBUF];                        // per epilogue warp, two blocks in flight
-    uint64_t full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC];
+    uint64_t full[P::STAGES], empty[P::STAGES], acc_full[NACC], acc_empty[NACC];
     uint32_t tmem_base;
     int abort;
 };
-static_assert(STAGE_BYTES % 1024 == 0 && TILE_A % 1024 == 0 && TILE_B % 1024 == 0,
-              "swizzled tiles start on 1024-byte boundaries");
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
 {
@@ -94,18 +109,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// the 64-byte swizzle: rows of 64 bytes (32 bf16 along K), atoms of 8 rows
-// (512 bytes, the stride between 8-row groups); the leading-dimension offset
-// is not used by this layout.  Bits: start address >> 4 [0, 14), leading byte
-// offset >> 4 [16, 30), stride byte offset >> 4 [32, 46), descriptor version 1
-// [46, 48), swizzle mode [61, 64) (4: 64-byte).  (K steps of 64 with the
-// 128-byte swizzle and two 96 KB stages were ~7 % slower on the layer's
-// products: half as many stages in flight.)
-__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr)
+// the swizzle of its row width (BK bf16 = 64 or 128 bytes): atoms of 8 rows,
+// SBO bytes apart; the leading-dimension offset is not used by these layouts.
+// Bits: start address >> 4 [0, 14), leading byte offset >> 4 [16, 30), stride
+// byte offset >> 4 [32, 46), descriptor version 1 [46, 48), swizzle mode
+// [61, 64) (2: 128-byte, 4: 64-byte).
+template <class P>
+__device__ __forceinline__ uint64_t tile_desc(uint32_t saddr)
 {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(4) << 61);
+           (static_cast<uint64_t>(P::SBO >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (P::SWZ << 61);
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
@@ -162,7 +175,7 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo)
     lo = x - hi;
 }
 
-template <int EPI>
+template <int EPI, class P>
 __global__ void __launch_bounds__(NTHREADS, 1)
     ffgemm_kernel(const __grid_constant__ CUtensorMap ta_hi, const __grid_constant__ CUtensorMap ta_lo,
                   const __grid_constant__ CUtensorMap tb_hi, const __grid_constant__ CUtensorMap tb_lo,
@@ -170,7 +183,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   const GemmArgs ga)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    constexpr int BK = P::BK, STAGES = P::STAGES, TILE_A = P::TILE_A, TILE_B = P::TILE_B;
+    constexpr int STAGE_BYTES = P::STAGE_BYTES;
+    Smem<P>& sm = *reinterpret_cast<Smem<P>*>(smem_raw);
     if ((smem_u32(smem_raw) & 1023u) != 0) {   // the swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicOr(ga.status, kStatusSmemBase);
         return;
@@ -273,9 +288,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint32_t ko = static_cast<uint32_t>(k * 32);   // 16 bf16 along K
-                    const uint64_t a_hi = sw64_desc(base + ko), a_lo = sw64_desc(base + TILE_A + ko);
-                    const uint64_t b_hi = sw64_desc(base + 2 * TILE_A + ko);
-                    const uint64_t b_lo = sw64_desc(base + 2 * TILE_A + TILE_B + ko);
+                    const uint64_t a_hi = tile_desc<P>(base + ko), a_lo = tile_desc<P>(base + TILE_A + ko);
+                    const uint64_t b_hi = tile_desc<P>(base + 2 * TILE_A + ko);
+                    const uint64_t b_lo = tile_desc<P>(base + 2 * TILE_A + TILE_B + ko);
                     umma(d, a_hi, b_hi, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma(d, a_hi, b_lo, idesc, 1u);
                     umma(d, a_lo, b_hi, idesc, 1u);
@@ -418,17 +433,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 }
 
 // 2-D map over a row-major bf16 [rows, K] matrix: boxes of `box_rows` rows x
-// 32 columns, 64-byte swizzle, zero fill outside the matrix.
-int make_map(CUtensorMap* map, const void* base, long long rows, int K, int box_rows)
+// bk columns, the swizzle of the box row (64 or 128 bytes), zero fill outside
+// the matrix.
+int make_map(CUtensorMap* map, const void* base, long long rows, int K, int box_rows, int bk)
 {
     auto enc = encoder();
     if (!enc) return SRWM_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SRWM_OK : SRWM_ERR_CUDA;
 }
@@ -468,12 +485,13 @@ int ff_gemm(int epi, const void* a_hi, const void* a_lo, const void* b_hi, const
     using namespace ff;
     if (args.N <= 0 || args.Mo <= 0) return SRWM_OK;
     if (args.K <= 0 || args.K % 8 != 0 || args.Mo % 8 != 0) return SRWM_ERR_UNSUPPORTED;
+    const int bk = args.K <= 1024 ? 64 : 32;
     CUtensorMap m[6];
     int rc;
-    if ((rc = make_map(&m[0], a_hi, args.N, args.K, BM)) != SRWM_OK ||
-        (rc = make_map(&m[1], a_lo, args.N, args.K, BM)) != SRWM_OK ||
-        (rc = make_map(&m[2], b_hi, args.Mo, args.K, BN)) != SRWM_OK ||
-        (rc = make_map(&m[3], b_lo, args.Mo, args.K, BN)) != SRWM_OK)
+    if ((rc = make_map(&m[0], a_hi, args.N, args.K, BM, bk)) != SRWM_OK ||
+        (rc = make_map(&m[1], a_lo, args.N, args.K, BM, bk)) != SRWM_OK ||
+        (rc = make_map(&m[2], b_hi, args.Mo, args.K, BN, bk)) != SRWM_OK ||
+        (rc = make_map(&m[3], b_lo, args.Mo, args.K, BN, bk)) != SRWM_OK)
         return rc;
     if (epi == 1) {
         if ((rc = make_out_map(&m[4], args.out_hi, args.N, args.Mo, false)) != SRWM_OK ||
@@ -483,9 +501,11 @@ int ff_gemm(int epi, const void* a_hi, const void* a_lo, const void* b_hi, const
         if ((rc = make_out_map(&m[4], args.out, args.N, args.Mo, true)) != SRWM_OK) return rc;
         m[5] = m[4];
     }
-    const void* kern = epi == 1 ? reinterpret_cast<const void*>(&ffgemm_kernel<1>)
-                                : reinterpret_cast<const void*>(&ffgemm_kernel<2>);
-    const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+    const void* kern = bk == 64 ? (epi == 1 ? reinterpret_cast<const void*>(&ffgemm_kernel<1, Pipe<64>>)
+                                            : reinterpret_cast<const void*>(&ffgemm_kernel<2, Pipe<64>>))
+                                : (epi == 1 ? reinterpret_cast<const void*>(&ffgemm_kernel<1, Pipe<32>>)
+                                            : reinterpret_cast<const void*>(&ffgemm_kernel<2, Pipe<32>>));
+    const int smem = static_cast<int>(bk == 64 ? sizeof(Smem<Pipe<64>>) : sizeof(Smem<Pipe<32>>)) + 1024;
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
