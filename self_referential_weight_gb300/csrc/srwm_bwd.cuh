@@ -30,7 +30,10 @@
 // D/4 columns of float4 chunks cg + 4 j.  Row dot products finish with two xor
 // shuffles over the four column groups; column sums over rows finish with a
 // transposed butterfly over the eight row groups of a warp and a fixed-order
-// sum over warps in shared memory, so the result is deterministic.
+// sum over warps in shared memory, so the result is deterministic.  A step's
+// W^T dz (its dL/dx~) is summed inside the next step's column sum, with that
+// step's two vectors, so a step takes two CTA barriers; the last step of a
+// segment sums its own.
 #pragma once
 
 #include <cuda.h>
@@ -89,6 +92,7 @@ struct BwdCfg {
     static constexpr int RS = emit_record_floats(D, NLR);   // floats per record
     static constexpr int NV2 = 2 * CPT;          // values of a two-vector column reduction
     static constexpr int NV1 = CPT < 8 ? 8 : CPT;  // one-vector reduction (padded to 8)
+    static constexpr int NV3 = NV2 + NV1;        // two vectors and one carried (padded)
 };
 
 template <class C>
@@ -99,8 +103,8 @@ struct __align__(128) BwdSmem {
     float xs[2][C::KSEG][C::D];
     float dyv[2][C::KSEG][C::D];
     uint64_t bar[2];             // "segment landed", by buffer
-    float red[C::NW][2][C::D];   // per-warp column partials
-    float vec[2][C::D];          // column sums
+    float red[C::NW][3][C::D];   // per-warp column partials
+    float vec[3][C::D];          // column sums
     float bred[C::NW][4];        // per-warp block sums of dcoef a
     float bsum[4];               // their sums over warps
 };
@@ -281,15 +285,15 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
     // colsum with two vectors, plus four block sums (bs: per-thread partials):
     // afterwards sm.vec[0..1] hold the column sums and sm.bsum[0..3] the
     // block sums, all in a fixed order of warps (deterministic)
-    auto colsum_gate = [&](float (&v)[C::NV2], float (&bsum4)[4]) {
-        constexpr int N = C::NV2;
+    auto colsum_gate = [&](float (&v)[C::NV3], float (&bsum4)[4]) {
+        constexpr int N = C::NV3;
         rowgroup_reduce<N>(v, lane);
         const int rg_lo = (lane >> 2) & 7;
 #pragma unroll
         for (int e = 0; e < N / 8; ++e) {
             const int idx = rg_lo * (N / 8) + e;
             const int vv = idx / CPT, q = idx - vv * CPT;
-            sm.red[warp][vv][bcol<C>(cg, q)] = v[e];
+            if (vv < 3) sm.red[warp][vv][bcol<C>(cg, q)] = v[e];
         }
         // the block sums over the warp's 32 lanes: two transposed levels,
         // then three plain ones; lane bits (4, 3) select the block
@@ -308,15 +312,15 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
             if ((lane & 7) == 0) sm.bred[warp][lane >> 3] = k;
         }
         __syncthreads();
-        for (int idx = tid; idx < 2 * D + 4; idx += C::NT) {
+        for (int idx = tid; idx < 3 * D + 4; idx += C::NT) {
             float acc = 0.f;
-            if (idx < 2 * D) {
+            if (idx < 3 * D) {
                 const int vv = idx / D, c = idx - vv * D;
                 for (int ww = 0; ww < C::NW; ++ww) acc += sm.red[ww][vv][c];
                 sm.vec[vv][c] = acc;
             } else {
-                for (int ww = 0; ww < C::NW; ++ww) acc += sm.bred[ww][idx - 2 * D];
-                sm.bsum[idx - 2 * D] = acc;
+                for (int ww = 0; ww < C::NW; ++ww) acc += sm.bred[ww][idx - 3 * D];
+                sm.bsum[idx - 3 * D] = acc;
             }
         }
         __syncthreads();
@@ -397,6 +401,26 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
         // the next segment (earlier steps) into the other buffer
         if (t0 > t_lo) issue(max(t_lo, t0 - KSEG), min(KSEG, t0 - t_lo));
         const float* rec = &sm.rec[buf][0][0];
+        // dL/dx of step s of this segment from the column sums in sm.vec[vv]
+        // (through the input softmax when present)
+        auto write_dx = [&](int s, int vv) {
+            const size_t gx = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
+            if (softmax_input) {
+                if (warp == 0) {
+                    const float* dxv = sm.vec[vv];
+                    float dot = 0.f;
+                    for (int c = lane; c < D; c += 32) dot = fmaf(sm.xs[buf][s][c], dxv[c], dot);
+                    dot = group_sum<32>(dot);
+                    for (int c = lane; c < D; c += 32) bp.dx[gx + c] = sm.xs[buf][s][c] * (dxv[c] - dot);
+                }
+            } else if (tid < D) {
+                bp.dx[gx + tid] = sm.vec[vv][tid];
+            }
+        };
+        // W^T dz partials of the step before (summed in this step's column sum)
+        float cxp[C::NV1];
+#pragma unroll
+        for (int q = 0; q < C::NV1; ++q) cxp[q] = 0.f;
         auto pk_of = [&](int s) { return rec + s * C::RS; };
         auto u_of = [&](int s) { return rec + s * C::RS + D; };
         auto g_of = [&](int s, int blkidx) { return rec[s * C::RS + 2 * D + blkidx]; };
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
             // 2. column sums v1 = dW'^T coef, v2 = W^T da, and the gate
             // gradients' block sums of dcoef a (slot i is block i here)
             float da[S];
-            float cv[C::NV2];
+            float cv[C::NV3];
             float bs[4];
             {
                 float2 c1[CP], c2[CP];
@@ -454,12 +478,16 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                     cv[CPT + 2 * q] = c2[q].x;
                     cv[CPT + 2 * q + 1] = c2[q].y;
                 }
+#pragma unroll
+                for (int q = 0; q < C::NV1; ++q) cv[C::NV2 + q] = cxp[q];
             }
             if constexpr (NLR == 1) {
                 bs[0] = (bs[0] + bs[1]) + (bs[2] + bs[3]);
                 bs[1] = bs[2] = bs[3] = 0.f;
             }
-            colsum_gate(cv, bs);   // sm.vec[0] = v1, sm.vec[1] = v2, sm.bsum[j] = block j's sum
+            // sm.vec[0] = v1, sm.vec[1] = v2, sm.vec[2] = dx~ of step s + 1, sm.bsum[j] = block j's sum
+            colsum_gate(cv, bs);
+            if (s + 1 < len) write_dx(s + 1, 2);
             // 3. dz for this thread's rows: y row dy; k, q rows through the
             // softmax backward; beta row through the sigmoid
             float dz[S];
@@ -485,7 +513,6 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                 }
             }
             // 4. dW += da (outer) u + dz (outer) x~ ; column partials of W^T dz
-            float cx[C::NV1];
             {
                 float2 c3[CP];
 #pragma unroll
@@ -502,30 +529,15 @@ __global__ void __launch_bounds__(BwdCfg<D, NLR>::NT, bwd_ctas_per_sm<D>())
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < C::NV1; ++q) cx[q] = 0.f;
-#pragma unroll
                 for (int q = 0; q < CP; ++q) {
-                    cx[2 * q] = c3[q].x;
-                    cx[2 * q + 1] = c3[q].y;
+                    cxp[2 * q] = c3[q].x;
+                    cxp[2 * q + 1] = c3[q].y;
                 }
-            }
-            colsum(cx, 1);   // sm.vec[0] = dx~
-            // 5. dx (through the input softmax when present).  No barrier
-            // follows: sm.vec and sm.red are next written after the next
-            // column sum's first barrier, which these readers reach first.
-            const size_t gx = ((static_cast<size_t>(b) * T + t0 + s) * bp.H + h) * D;
-            if (softmax_input) {
-                if (warp == 0) {
-                    const float* dxv = sm.vec[0];
-                    float dot = 0.f;
-                    for (int c = lane; c < D; c += 32) dot = fmaf(sm.xs[buf][s][c], dxv[c], dot);
-                    dot = group_sum<32>(dot);
-                    for (int c = lane; c < D; c += 32) bp.dx[gx + c] = sm.xs[buf][s][c] * (dxv[c] - dot);
-                }
-            } else if (tid < D) {
-                bp.dx[gx + tid] = sm.vec[0][tid];
             }
         }
+        // the segment's last step (its earliest): its own column sum
+        colsum(cxp, 1);   // sm.vec[0] = dx~ of step 0
+        write_dx(0, 0);
         // the segment's buffer is read before copies into it (two segments on)
         fence_proxy_async_smem();
         __syncthreads();
