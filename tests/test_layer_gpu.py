@@ -94,11 +94,15 @@ def test_layer_tensor_core_products_agree_with_cublaslt():
 
 
 @pytest.mark.parametrize("B,T,H,d,d_ff", [(1, 1, 2, 16, 8), (3, 45, 8, 64, 2048), (2, 33, 2, 32, 24),
-                                          (1, 129, 4, 16, 64)])
+                                          (1, 129, 4, 16, 64), (2, 37, 3, 16, 1032)])
 def test_layer_tile_edges(B, T, H, d, d_ff):
     """Shapes at the tensor-core products' tile edges: one token, token
     counts off the 128-row tiles, hidden widths below one 256-column tile
-    and inner dimensions below one 64-wide K step (filled with zeros by TMA)."""
+    and inner dimensions below one K step (filled with zeros by TMA).  The
+    last case takes both K-step configurations at ragged edges: K = 48
+    (one 64-wide step, zero-filled), an output width of 1032 (a partial
+    256-column tile, 32-column stores clipped), and K = 1032 for the second
+    product (32-wide steps, the last one partial)."""
     n_lr = 4
     p = inputs.make_layer_params(H, d, n_lr, d_ff, 250 + T)
     u = inputs.make_layer_input(B, T, H * d, 250 + T)
