@@ -281,7 +281,7 @@ size_t srwm_backward_workspace_bytes(int B, int T, int H, int d, int n_lr);
  *   workspace  device scratch of srwm_layer_workspace_bytes(...) bytes,
  *              16-byte aligned, untouched until the work on `stream` ends
  *
- * Supported: D = H*d <= 1024, d_ff a positive multiple of 4, and the
+ * Supported: D = H*d <= 1024, d_ff a positive multiple of 8, and the
  * srwm_forward limits.  The same pointer rules apply: outputs and workspace
  * overlap nothing else.
  */
